@@ -1,0 +1,465 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV-cache attention hot path; prints ONE JSON line.
+
+A step is one pass of the decode hot path over one batch: pa_write_kv of the
+batch's new K/V rows through slot_mapping, then pa_decode (split-KV
+partition kernel + merge kernel) reading every visible token through the
+block tables.  The default workload is the GQA decode batch (64 sequences,
+H_q 32 / H_kv 8, head_dim 128, block size 16, bf16, contexts U[128, 4096]).
+``--workload prefill`` times pa_write_kv + pa_prefill instead.
+
+Timing: W untimed warm-up steps; then K steps, each preceded (outside its
+events) by a 256 MiB write that flushes L2, each bracketed by CUDA events on
+the launching stream; barrier + synchronize around the loop; max over ranks.
+value = algorithmic bytes of all ranks / max step time (GB/s).  The
+algorithmic bytes of a decode step are the K/V rows of every visible token,
+Q, the fp32 output, the block-table entries and context lengths.
+
+--impl reference times the float64 CPU oracle on the host cores instead (the
+only other code this script may run from oracle/).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode KV-read GB/s (% of HBM peak) and decode tokens/s on 1 GB300"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_gqa", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic_bytes(wl) -> dict:
+    """Bytes one decode (or prefill) step must move at minimum."""
+    e = wl.elem_bytes
+    n = wl.total_lens.astype(np.int64)
+    kv = int(n.sum()) * wl.logical_bytes_per_token()
+    tables = int((-(-n // wl.block_size)).sum()) * 4
+    n_q = int(wl.new_lens.sum())
+    q = n_q * wl.num_q_heads * wl.head_dim * e
+    out = n_q * wl.num_q_heads * wl.head_dim * 4
+    lens = wl.num_seqs * 4
+    write = n_q * wl.num_kv_heads * wl.head_dim * e * 2 * 2 + n_q * 8
+    return {"kv": kv, "q": q, "out": out, "tables": tables, "lens": lens, "write": write,
+            "decode_total": kv + q + out + tables + lens}
+
+
+def prefill_flops(wl) -> float:
+    """Causal-visible flops of one prefill pass: 4*D per (query, head, visible key)."""
+    tot = 0
+    for s in range(wl.num_seqs):
+        c, m = int(wl.cached_lens[s]), int(wl.new_lens[s])
+        vis = (c + 1 + np.arange(m)) if wl.causal else np.full(m, c + m)
+        tot += int(vis.sum())
+    return 4.0 * wl.head_dim * wl.num_q_heads * tot
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) while the timed loop runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- traffic record
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("decode.cu", "common.cuh", "prefill.cu", "write_copy.cu"):
+        p = os.path.join(ROOT, "paged_kv_cache_148_gb300", "csrc", f)
+        if os.path.exists(p):
+            with open(p, "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        rec = d[kernel][workload]
+        if rec.get("source_hash") == kernel_source_hash():
+            return int(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def cpu_oracle_run(wl, seconds: float):
+    """Time the float64 oracle on the host cores over a bounded sample of the batch."""
+    import oracle
+    oc = oracle.OracleCache(wl)
+    q = oracle.to_numpy_bits(wl.queries())
+    t_budget = seconds
+    if wl.kind == "decode":
+        # sequences in batch order until ~t_budget of work, measured by doing it
+        done_bytes, elapsed, s = 0, 0.0, 0
+        per_tok = wl.logical_bytes_per_token()
+        while s < wl.num_seqs and elapsed < t_budget:
+            rows = [(s, g) for g in range(wl.num_q_heads)]
+            t0 = time.perf_counter()
+            oracle.decode(oc.k, oc.v, q, oc.tables, wl.total_lens, wl.scale, rows=rows)
+            elapsed += time.perf_counter() - t0
+            n = int(wl.total_lens[s])
+            done_bytes += (n * per_tok + wl.num_q_heads * wl.head_dim * (wl.elem_bytes + 4)
+                           + 4 * (-(-n // wl.block_size)) + 4)
+            s += 1
+        return {"value": done_bytes / elapsed / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+                "kind": "oracle",
+                "sample": "float64 oracle decode of the first %d of %d sequences (all %d q-heads), "
+                          "%.1f s" % (s, wl.num_seqs, wl.num_q_heads, elapsed),
+                "seconds": elapsed, "tokens_per_s": s / elapsed}
+    # prefill: a sample of (token, head) rows, scaled to TFLOP/s of visible work
+    cu = np.concatenate([[0], np.cumsum(wl.new_lens)])
+    rng = np.random.default_rng(0)
+    T = int(cu[-1])
+    rows, flops, elapsed = [], 0.0, 0.0
+    while elapsed < t_budget and len(rows) < 1 << 16:
+        batch = [(int(t), int(h)) for t, h in zip(rng.integers(0, T, 64),
+                                                  rng.integers(0, wl.num_q_heads, 64))]
+        t0 = time.perf_counter()
+        oracle.prefill(oc.k, oc.v, q, cu, wl.total_lens, oc.tables, wl.scale, wl.causal, rows=batch)
+        elapsed += time.perf_counter() - t0
+        for t, h in batch:
+            s = int(np.searchsorted(cu, t, side="right") - 1)
+            pos = int(wl.cached_lens[s]) + (t - int(cu[s]))
+            flops += 4.0 * wl.head_dim * (pos + 1)
+        rows += batch
+    return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "float64 oracle prefill of %d random (token, q-head) rows, %.1f s"
+                      % (len(rows), elapsed), "seconds": elapsed}
+
+
+def reference_steps(wl, warmup: int, steps: int, budget_s: float):
+    """The oracle as the reference arm: each step decodes one sequence of the
+    batch (all q-heads) in float64, cycling through the batch; the timed steps
+    stop early if the time budget runs out."""
+    import oracle
+    oc = oracle.OracleCache(wl)
+    q = oracle.to_numpy_bits(wl.queries())
+    per_tok = wl.logical_bytes_per_token()
+    if wl.kind != "decode":
+        r = cpu_oracle_run(wl, min(budget_s, 30.0))
+        r.update({"steps": 1, "ms_per_step": r["seconds"] * 1e3})
+        return r
+    def one(s):
+        rows = [(s, g) for g in range(wl.num_q_heads)]
+        oracle.decode(oc.k, oc.v, q, oc.tables, wl.total_lens, wl.scale, rows=rows)
+        n = int(wl.total_lens[s])
+        return (n * per_tok + wl.num_q_heads * wl.head_dim * (wl.elem_bytes + 4)
+                + 4 * (-(-n // wl.block_size)) + 4)
+    for i in range(warmup):
+        one(i % wl.num_seqs)
+    done, nbytes, t0 = 0, 0, time.perf_counter()
+    while done < max(1, steps) and time.perf_counter() - t0 < budget_s:
+        nbytes += one((warmup + done) % wl.num_seqs)
+        done += 1
+    el = time.perf_counter() - t0
+    return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "steps": done, "ms_per_step": el / done * 1e3,
+            "sample": "float64 oracle, one sequence (all %d q-heads) per step, %d steps in %.1f s"
+                      % (wl.num_q_heads, done, el)}
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import paged_kv_cache_148_gb300 as pkv
+    from harness import GpuWorkload
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pkv.build()
+    wl = workloads.WORKLOADS[args.workload]()
+    g = GpuWorkload(wl, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    is_decode = wl.kind == "decode"
+    max_parts = g.max_parts()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        g.write_new(stream)
+        if is_decode:
+            g.attend(stream, "partial")
+            g.attend(stream, "merge")
+        else:
+            g.attend(stream)
+
+    for i in range(args.warmup):
+        flush.fill_(i & 255)
+        step()
+    torch.cuda.synchronize(dev)
+    g.err.zero_()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    for i in range(K):
+        flush.fill_(i & 255)
+        e = ev[i]
+        e[0].record(stream)
+        g.write_new(stream)
+        e[1].record(stream)
+        if is_decode:
+            g.attend(stream, "partial")
+            e[2].record(stream)
+            g.attend(stream, "merge")
+        else:
+            g.attend(stream)
+            e[2].record(stream)
+        e[3].record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    err = int(g.err.item())
+    if err:
+        raise RuntimeError("device error during the timed loop: " + pkv.status_str(err))
+    step_ms = np.array([e[0].elapsed_time(e[3]) for e in ev])
+    write_ms = np.array([e[0].elapsed_time(e[1]) for e in ev])
+    attn_ms = np.array([e[1].elapsed_time(e[2]) for e in ev])
+    merge_ms = np.array([e[2].elapsed_time(e[3]) for e in ev])
+    ms = float(step_ms.mean())
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end-to-end through the public API with host buffers
+    e2e = run_e2e(args, g, stream, dev, is_decode)
+
+    hbm_peak, tf_peak, peak_src = measured_peaks()
+    ab = algorithmic_bytes(wl)
+    res = {"metric": METRIC, "n_gpus": world, "steps": K, "warmup": args.warmup,
+           "ms_per_step": ms, "scaling": "weak", "vs_baseline": None, "data": "synthetic",
+           "dtype": wl.dtype}
+    cfg = {"workload": wl.name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+           "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+           "block_size": wl.block_size, "num_blocks": wl.num_blocks,
+           "context_lens": "sum %d, min %d, max %d" % (int(wl.total_lens.sum()),
+                                                      int(wl.total_lens.min()),
+                                                      int(wl.total_lens.max())),
+           "per_rank": "each rank runs its own copy of the batch (independent replicas)",
+           "l2": "flushed before every timed step by a 256 MiB write outside the step's events",
+           "split_kv_partitions_max": max_parts}
+    if is_decode:
+        per_rank = ab["decode_total"]
+        res.update({"value": world * per_rank / (ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "higher_is_better": True,
+                    "tokens_per_s": world * wl.num_seqs / (ms * 1e-3),
+                    "pct_of_hbm_peak": 100.0 * (per_rank / (ms * 1e-3) / 1e9) / hbm_peak,
+                    "pct_of_nominal_8tbs": 100.0 * (per_rank / (ms * 1e-3) / 1e9) / 8000.0})
+        part_ms = float(attn_ms.mean())
+        achieved = per_rank / (part_ms * 1e-3) / 1e9
+        res["roofline"] = {"kernel": "decode_partition_kernel", "bound": "hbm",
+                           "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                           "frac": achieved / hbm_peak, "peak_source": peak_src + " hbm_gbs",
+                           "traffic": recorded_traffic("decode_partition_kernel", wl.name),
+                           "algorithmic_bytes": per_rank, "launch_ms": part_ms}
+        res["kernel_ms"] = {"write_kv": float(write_ms.mean()),
+                            "decode_partition": part_ms, "decode_merge": float(merge_ms.mean())}
+        launches = K * (2 + (1 if max_parts > 1 else 0))
+    else:
+        flops = prefill_flops(wl)
+        res.update({"metric": "paged chunked-prefill TFLOP/s (causal-visible) on 1 GB300",
+                    "value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "higher_is_better": True,
+                    "tokens_per_s": world * int(wl.new_lens.sum()) / (ms * 1e-3)})
+        pf_ms = float(attn_ms.mean())
+        achieved = flops / (pf_ms * 1e-3) / 1e12
+        res["roofline"] = {"kernel": "prefill_kernel", "bound": "tensor", "achieved": achieved,
+                           "peak": tf_peak, "unit": "TFLOP/s", "frac": achieved / tf_peak,
+                           "peak_source": peak_src + " bf16_tflops (burst)",
+                           "traffic": recorded_traffic("prefill_kernel", wl.name),
+                           "algorithmic_flops": flops, "launch_ms": pf_ms}
+        res["kernel_ms"] = {"write_kv": float(write_ms.mean()), "prefill": pf_ms}
+        launches = K * 2
+    res["gpu_launches"] = launches
+    res["e2e"] = e2e
+    res["clocks"] = clk
+    res["config"] = cfg
+    return res, wl, ab
+
+
+def run_e2e(args, g, stream, dev, is_decode):
+    """Same step through the public API with pinned host buffers, copies timed."""
+    import torch
+    wl = g.wl
+    host_in = {"q": g.q_host, "k_new": g.k_new_host, "v_new": g.v_new_host,
+               "slot_mapping": torch.from_numpy(g.slot_mapping_host),
+               "block_tables": g.block_tables.cpu(), "context_lens": g.context_lens.cpu()}
+    if not is_decode:
+        host_in["cu_seqlens_q"] = g.cu_seqlens_q.cpu()
+    pinned = {k: v.contiguous().pin_memory() for k, v in host_in.items()}
+    out_host = torch.empty(g.out.shape, dtype=g.out.dtype).pin_memory()
+    dev_bufs = {"q": g.q, "k_new": g.k_new, "v_new": g.v_new, "slot_mapping": g.slot_mapping,
+                "block_tables": g.block_tables, "context_lens": g.context_lens}
+    if not is_decode:
+        dev_bufs["cu_seqlens_q"] = g.cu_seqlens_q
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = out_host.numel() * out_host.element_size()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def one():
+        for k, t in pinned.items():
+            dev_bufs[k].copy_(t, non_blocking=True)
+        g.step(stream)
+        out_host.copy_(g.out, non_blocking=True)
+
+    for i in range(3):
+        one()
+    torch.cuda.synchronize(dev)
+    n = max(1, args.e2e_steps)
+    ms = []
+    for i in range(n):
+        flush.fill_(i & 255)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one()
+        b.record(stream)
+        ms.append((a, b))
+    torch.cuda.synchronize(dev)
+    t = float(np.mean([a.elapsed_time(b) for a, b in ms]))
+    if is_decode:
+        val, unit = algorithmic_bytes(wl)["decode_total"] / (t * 1e-3) / 1e9, "GB/s"
+    else:
+        val, unit = prefill_flops(wl) / (t * 1e-3) / 1e12, "TFLOP/s"
+    return {"value": val, "unit": unit, "ms_per_step": t, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        wl = workloads.WORKLOADS[args.workload]()
+        cpu = reference_steps(wl, args.warmup, args.steps, budget_s=150.0)
+        line = {"impl": "reference", "metric": METRIC if wl.kind == "decode" else
+                "paged chunked-prefill TFLOP/s (causal-visible) on 1 GB300",
+                "value": cpu["value"], "unit": cpu["unit"], "higher_is_better": True,
+                "n_gpus": world, "steps": cpu["steps"], "warmup": args.warmup,
+                "ms_per_step": cpu["ms_per_step"], "data": "synthetic", "dtype": "f64",
+                "scaling": "weak", "vs_baseline": None, "config": {"workload": wl.name},
+                "cpu_baseline": {"value": cpu["value"], "unit": cpu["unit"], "cores": cpu["cores"],
+                                 "kind": "oracle", "sample": cpu["sample"]},
+                "e2e": {"value": cpu["value"], "unit": cpu["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl")
+    res, wl, ab = run_ours(args, rank, world, local_rank)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_run(wl, args.cpu_seconds)
+        res["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    elif rank == 0:
+        res["cpu_baseline"] = None
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,713 @@
+// pa_decode: paged decode attention with split-KV partitions and a merge.
+//
+// Semantics: the pseudo-kernel and backend rules of "03｜PagedAttention 与 KV
+// Cache 内存系统" §4 — for every (sequence, query head) walk the visible logical
+// blocks, look the physical block up in the table, attend to the page and
+// combine blockwise softmax states (max, exp_sum, weighted value); the lookup
+// is fused into the kernel, long contexts are split into partitions whose
+// states are merged by a second kernel.
+//
+// Design (sm_103a, HBM-bound):
+//  * One CTA = (sequence, kv-head, partition).  All G = H_q / H_kv query heads
+//    of the group share every K/V byte read (GQA mapping g -> g / G).
+//  * A warp owns every W-th 16-token chunk of the partition and streams them
+//    through its own S-stage ring in shared memory with 1-D bulk copies (TMA
+//    engine) completing on an mbarrier: 4 KiB of K and 4 KiB of V per chunk,
+//    one contiguous run of a (block, kv-head) page.  Lane 0 is the producer;
+//    block-table entries for the next 32 chunks are prefetched one per lane.
+//  * Scores: lanes split the 256-byte row into 16-byte columns (16 lanes per
+//    row, two rows per warp access, conflict-free LDS.128).  The partial dot
+//    products of 8 tokens x G heads are finished by a transpose-reduction
+//    over 4 shuffle rounds in which every round halves the live values; each
+//    lane's token/head order is permuted (by XOR with its lane bits) so the
+//    rounds need no selects.  Afterwards a lane holds G/2 finished scores.
+//  * Softmax in base 2 (scores carry scale*log2 e); the running max is only
+//    raised when a score exceeds it by more than 2^8, so rescaling the
+//    accumulators is rare; the result is unchanged because the shift cancels
+//    in the final division.
+//  * P*V: probabilities go through a 16xG shared buffer; lanes accumulate
+//    acc[g][d] over their 8 rows for their 16-byte column; the two row halves
+//    are added at the end.
+//  * The CTA's warps combine in shared memory; a single-partition sequence
+//    writes the normalised output directly, otherwise (m, l, acc) partials go
+//    to the workspace and decode_merge_kernel finishes.
+#include <cfloat>
+#include <cmath>
+
+#include "common.cuh"
+#include "host_common.h"
+
+namespace pa {
+
+constexpr int kChunk = 16;                        // tokens per ring stage
+constexpr int kRowBytes = 256;                    // head_dim * element bytes
+constexpr int kChunkBytes = kChunk * kRowBytes;   // 4 KiB of K (and of V) per stage
+constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale when max grows > 256x
+constexpr unsigned kFull = 0xffffffffu;
+
+struct DecodeParams {
+    const unsigned char* k_pool;
+    const unsigned char* v_pool;
+    int32_t num_blocks;
+    int32_t log2_bp;
+    int32_t num_kv_heads;
+    const void* q;
+    int32_t num_q_heads;
+    const int32_t* block_tables;
+    int32_t max_blocks;
+    const int32_t* context_lens;
+    float scale_log2;
+    int32_t part_chunks;
+    int32_t max_parts;
+    float* out;
+    float* ws_m;
+    float* ws_l;
+    float* ws_acc;
+    int32_t* d_err;
+};
+
+template <typename T>
+struct Row;
+template <>
+struct Row<float> {
+    static constexpr int N = 4;  // elements per 16-byte column
+    static PA_DEVICE void unpack(const uint4& u, float (&f)[4]) {
+        f[0] = __uint_as_float(u.x);
+        f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z);
+        f[3] = __uint_as_float(u.w);
+    }
+};
+template <>
+struct Row<uint16_t> {  // bf16 bit patterns
+    static constexpr int N = 8;
+    static PA_DEVICE void unpack(const uint4& u, float (&f)[8]) {
+        f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
+        f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+        f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
+        f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+    }
+};
+
+template <int W, int S, int G>
+struct DecodeSmem {
+    static constexpr size_t ring = (size_t)W * S * 2 * kChunkBytes;
+    static constexpr size_t bars = ring;
+    static constexpr size_t masks = bars + (size_t)W * S * 8;
+    static constexpr size_t probs = masks + (size_t)W * S * 4;
+    static constexpr size_t total = probs + (size_t)W * kChunk * G * 4;
+    // the CTA combine reuses the ring: per warp 2G + G*D floats
+    static_assert((size_t)W * (4 * G + G * 128) * 4 <= ring, "combine area must fit in the ring");
+};
+
+// Producer side: lane 0 of a warp fetches chunk `c` (16 tokens starting at
+// c*16) of sequence s, kv-head h, into ring stage `kst` (K) / `kst +
+// kChunkBytes` (V).  Writes the valid-row mask, then arms the barrier.
+template <int W>
+PA_DEVICE void issue_chunk(const DecodeParams& p, int s, int h, int n, int c, int32_t id_first,
+                           unsigned char* kst, uint64_t* bar, uint32_t* mask_slot) {
+    const int t0 = c * kChunk;
+    const int bp = 1 << p.log2_bp;
+    const int valid = min(kChunk, n - t0);
+    uint32_t mask = 0, bytes = 0;
+    const int64_t page_rows = (int64_t)bp;
+    if (bp >= kChunk) {
+        const int32_t id = id_first;
+        if (id < 0 || id >= p.num_blocks) {
+            set_error(p.d_err, id < 0 ? PA_ERR_NEGATIVE_BLOCK : PA_ERR_OUT_OF_RANGE);
+            *mask_slot = 0;
+            mbar_arrive_expect_tx(bar, 0);
+            return;
+        }
+        mask = (1u << valid) - 1u;  // valid <= 16
+        bytes = 2 * kChunkBytes;
+        const int64_t row0 = ((int64_t)id * p.num_kv_heads + h) * page_rows + (t0 & (bp - 1));
+        *mask_slot = mask;
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(kst, p.k_pool + row0 * kRowBytes, kChunkBytes, bar);
+        bulk_g2s(kst + kChunkBytes, p.v_pool + row0 * kRowBytes, kChunkBytes, bar);
+        return;
+    }
+    // block size below the chunk: 16 / bp pages per chunk
+    const int pages = kChunk >> p.log2_bp;
+    const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks;
+    const int e0 = t0 >> p.log2_bp;
+    int32_t ids[kChunk];
+#pragma unroll 1
+    for (int pp = 0; pp < pages; ++pp) {
+        ids[pp] = -1;
+        const int tok = t0 + pp * bp;
+        if (tok >= n) break;
+        const int e = e0 + pp;
+        const int32_t id = (e < p.max_blocks) ? __ldg(table + e) : -1;
+        if (e >= p.max_blocks || id >= p.num_blocks) {
+            set_error(p.d_err, PA_ERR_OUT_OF_RANGE);
+            continue;
+        }
+        if (id < 0) {
+            set_error(p.d_err, PA_ERR_NEGATIVE_BLOCK);
+            continue;
+        }
+        ids[pp] = id;
+        const int rows = min(bp, n - tok);
+        mask |= ((1u << rows) - 1u) << (pp * bp);
+        bytes += 2u * (uint32_t)bp * kRowBytes;
+    }
+    *mask_slot = mask;
+    mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll 1
+    for (int pp = 0; pp < pages; ++pp) {
+        if (t0 + pp * bp >= n) break;
+        if (ids[pp] < 0) continue;
+        const int64_t row0 = ((int64_t)ids[pp] * p.num_kv_heads + h) * page_rows;
+        const uint32_t nb = (uint32_t)bp * kRowBytes;
+        bulk_g2s(kst + pp * bp * kRowBytes, p.k_pool + row0 * kRowBytes, nb, bar);
+        bulk_g2s(kst + kChunkBytes + pp * bp * kRowBytes, p.v_pool + row0 * kRowBytes, nb, bar);
+    }
+}
+
+template <typename T, int G, int W, int S>
+__global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodeParams p) {
+    using R = Row<T>;
+    constexpr int EPL = R::N;                 // elements of a row per lane
+    constexpr int D = EPL * 16;               // head_dim
+    constexpr int LOG2G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+    constexpr int NS = 8 * G;                 // partial scores per lane: 8 rows x G heads
+    constexpr int ROUNDS = G == 1 ? 3 : 4;    // halving rounds of the transpose-reduce
+    constexpr int NSF = G == 1 ? 1 : G / 2;   // finished scores per lane
+    using L = DecodeSmem<W, S, G>;
+    static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group size");
+
+    const int s = blockIdx.x, h = blockIdx.y, part = blockIdx.z;
+    int n = __ldg(p.context_lens + s);
+    if (n > p.max_parts * p.part_chunks * kChunk) {  // longer than the plan's max_context
+        if (part == 0 && h == 0 && threadIdx.x == 0) set_error(p.d_err, PA_ERR_OUT_OF_RANGE);
+        n = p.max_parts * p.part_chunks * kChunk;
+    }
+    const int n_chunks = (n + kChunk - 1) / kChunk;
+    const int c_begin = part * p.part_chunks;
+    if (n <= 0 || c_begin >= n_chunks) return;
+    const int c_end = min(c_begin + p.part_chunks, n_chunks);
+    const int n_parts = (n_chunks + p.part_chunks - 1) / p.part_chunks;
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned char* ring = smem + (size_t)warp * S * 2 * kChunkBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars) + warp * S;
+    uint32_t* masks = reinterpret_cast<uint32_t*>(smem + L::masks) + warp * S;
+    float* ps = reinterpret_cast<float*>(smem + L::probs) + warp * kChunk * G;
+    __shared__ int aborted;
+    if (threadIdx.x == 0) aborted = 0;
+
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // this warp's chunks: c_begin + warp + i*W
+    const int first = c_begin + warp;
+    const int my_n = first < c_end ? (c_end - first + W - 1) / W : 0;
+    const bool big_pages = p.log2_bp >= 4;
+    const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks;
+
+    // block-table prefetch: lane j holds the id of local chunk (base + j)
+    auto table_id = [&](int i) -> int32_t {
+        const int c = first + i * W;
+        const int e = (c * kChunk) >> p.log2_bp;
+        return e < p.max_blocks ? __ldg(table + e) : -1;
+    };
+    int32_t id_reg = (big_pages && lane < my_n) ? table_id(lane) : -1;
+    int id_base = 0;
+
+    // the error check for the table width happens at issue time
+    auto issue = [&](int i, int32_t id) {
+        const int stage = i % S;
+        const int c = first + i * W;
+        if (big_pages && ((c * kChunk) >> p.log2_bp) >= p.max_blocks) id = p.num_blocks;  // flagged
+        issue_chunk<W>(p, s, h, n, c, id, ring + (size_t)stage * 2 * kChunkBytes, &bars[stage],
+                       &masks[stage]);
+    };
+
+    // prologue: first S chunks in flight
+#pragma unroll
+    for (int i = 0; i < S; ++i) {
+        const int32_t id = __shfl_sync(kFull, id_reg, i & 31);
+        if (lane == 0 && i < my_n) issue(i, id);
+    }
+
+    // per-lane constants of the transpose-reduce layout
+    const int half = lane >> 4;               // which row of a row pair
+    const int col = lane & 15;                // 16-byte column of the row
+    const int jx = (lane >> 1) & 7;           // local row j holds row 2*(j^jx)+half
+    const int gx = G == 1 ? 0 : (lane & 1) * (G / 2);  // local head g holds head g^gx
+    const int t_mine = 2 * jx + half;         // row of this lane's finished scores
+
+    // query registers, permuted by gx and pre-scaled into base-2 logits
+    float qreg[G][EPL];
+    {
+        const T* qb = reinterpret_cast<const T*>(p.q) +
+                      ((int64_t)s * p.num_q_heads + (int64_t)h * G) * D + col * EPL;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(qb + (int64_t)(g ^ gx) * D));
+            float f[EPL];
+            R::unpack(u, f);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) qreg[g][e] = f[e] * p.scale_log2;
+        }
+    }
+
+    float acc[G][EPL];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[g][e] = 0.f;
+    float m[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) m[g] = -INFINITY;
+    float l_lane[NSF];
+#pragma unroll
+    for (int x = 0; x < NSF; ++x) l_lane[x] = 0.f;
+
+    bool ok = true;
+#pragma unroll 1
+    for (int i = 0; i < my_n; ++i) {
+        const int stage = i % S;
+        const uint32_t parity = (uint32_t)(i / S) & 1u;
+        ok = mbar_wait(&bars[stage], parity, p.d_err);
+        if (!__all_sync(kFull, ok)) {
+            ok = false;
+            break;
+        }
+        const uint32_t vmask = masks[stage];
+        const bool masked = vmask != 0xffffu;
+        const unsigned char* kst = ring + (size_t)stage * 2 * kChunkBytes;
+        const unsigned char* vst = kst + kChunkBytes;
+
+        // ---- scores: partial dots over this lane's column, then transpose-reduce
+        float part[NS];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int row = 2 * (j ^ jx) + half;
+            const uint4 u = *reinterpret_cast<const uint4*>(kst + row * kRowBytes + col * 16);
+            float k[EPL];
+            R::unpack(u, k);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float a = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) a = fmaf(qreg[g][e], k[e], a);
+                part[j * G + g] = a;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r) {
+            const int hn = NS >> (r + 1);
+#pragma unroll
+            for (int x = 0; x < hn; ++x)
+                part[x] += __shfl_xor_sync(kFull, part[x + hn], 8 >> r);
+        }
+        if (G == 1) part[0] += __shfl_xor_sync(kFull, part[0], 1);
+
+        // ---- online softmax (base 2) with rare rescaling
+        const bool tvalid = !masked || ((vmask >> t_mine) & 1u);
+        float sc[NSF], mm[NSF];
+#pragma unroll
+        for (int x = 0; x < NSF; ++x) {
+            sc[x] = tvalid ? part[x] : -INFINITY;
+            mm[x] = G == 1 ? m[0] : ((lane & 1) ? m[G / 2 + x] : m[x]);
+        }
+        bool need = false;
+#pragma unroll
+        for (int x = 0; x < NSF; ++x) need |= sc[x] > mm[x] + kRescaleThreshold;
+        if (__any_sync(kFull, need)) {
+            float cm[NSF];
+#pragma unroll
+            for (int x = 0; x < NSF; ++x) cm[x] = sc[x];
+#pragma unroll
+            for (int off = 2; off <= 16; off <<= 1)
+#pragma unroll
+                for (int x = 0; x < NSF; ++x) cm[x] = fmaxf(cm[x], __shfl_xor_sync(kFull, cm[x], off));
+            float cmax[G];
+            if (G == 1) {
+                cmax[0] = cm[0];
+            } else {
+#pragma unroll
+                for (int x = 0; x < NSF; ++x) {
+                    const float o = __shfl_xor_sync(kFull, cm[x], 1);
+                    cmax[x] = (lane & 1) ? o : cm[x];
+                    cmax[G / 2 + x] = (lane & 1) ? cm[x] : o;
+                }
+            }
+            float corr[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float mn = fmaxf(m[g], cmax[g]);
+                corr[g] = ex2(m[g] - mn);
+                m[g] = mn;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[g][e] *= corr[g];
+            }
+#pragma unroll
+            for (int x = 0; x < NSF; ++x) {
+                l_lane[x] *= G == 1 ? corr[0] : ((lane & 1) ? corr[G / 2 + x] : corr[x]);
+                mm[x] = G == 1 ? m[0] : ((lane & 1) ? m[G / 2 + x] : m[x]);
+            }
+        }
+        float pr[NSF];
+#pragma unroll
+        for (int x = 0; x < NSF; ++x) {
+            pr[x] = tvalid ? ex2(sc[x] - mm[x]) : 0.f;
+            l_lane[x] += pr[x];
+        }
+
+        // ---- broadcast probabilities of the 16 rows x G heads
+        if (G == 1) {
+            if ((lane & 1) == 0) ps[t_mine] = pr[0];
+        } else {
+#pragma unroll
+            for (int x = 0; x < NSF; ++x) ps[t_mine * G + gx + x] = pr[x];
+        }
+        __syncwarp();
+
+        // ---- P * V over this lane's 8 rows and 16-byte column
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int row = 2 * j + half;
+            float pg[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) pg[g] = ps[row * G + g];
+            const uint4 u = *reinterpret_cast<const uint4*>(vst + row * kRowBytes + col * 16);
+            float v[EPL];
+            R::unpack(u, v);
+            if (masked && !((vmask >> row) & 1u)) {
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) v[e] = 0.f;  // unwritten rows may hold NaN
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pg[g], v[e], acc[g][e]);
+        }
+        __syncwarp();
+
+        // ---- refill this stage with chunk i + S
+        const int nxt = i + S;
+        if (big_pages && nxt - id_base >= 32) {
+            id_base += 32;
+            id_reg = (id_base + lane < my_n) ? table_id(id_base + lane) : -1;
+        }
+        const int32_t nid = big_pages ? __shfl_sync(kFull, id_reg, (nxt - id_base) & 31) : -1;
+        if (lane == 0 && nxt < my_n) issue(nxt, nid);
+    }
+    if (!ok) aborted = 1;
+
+    // ---- finish this warp's state
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[g][e] += __shfl_xor_sync(kFull, acc[g][e], 16);
+#pragma unroll
+    for (int off = 2; off <= 16; off <<= 1)
+#pragma unroll
+        for (int x = 0; x < NSF; ++x) l_lane[x] += __shfl_xor_sync(kFull, l_lane[x], off);
+    float lsum[G];
+    if (G == 1) {
+        lsum[0] = l_lane[0];
+    } else {
+#pragma unroll
+        for (int x = 0; x < NSF; ++x) {
+            const float o = __shfl_xor_sync(kFull, l_lane[x], 1);
+            lsum[x] = (lane & 1) ? o : l_lane[x];
+            lsum[G / 2 + x] = (lane & 1) ? l_lane[x] : o;
+        }
+    }
+
+    // ---- combine the CTA's warps (reusing the ring) and write
+    __syncthreads();
+    if (aborted) return;
+    // per warp: acc [G][D], then m [G], l [G]; the stride keeps float4 alignment
+    float* cw = reinterpret_cast<float*>(smem);
+    constexpr int MOFF = G * D, LOFF = G * D + G;
+    constexpr int WSTRIDE = G * D + ((2 * G + 3) / 4) * 4;
+    float* mine = cw + warp * WSTRIDE;
+    if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            mine[MOFF + g] = m[g];
+            mine[LOFF + g] = lsum[g];
+        }
+    }
+    if (lane < 16) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < EPL; e += 4)
+                *reinterpret_cast<float4*>(mine + g * D + col * EPL + e) =
+                    make_float4(acc[g][e], acc[g][e + 1], acc[g][e + 2], acc[g][e + 3]);
+    }
+    __syncthreads();
+    const int64_t qh0 = (int64_t)s * p.num_q_heads + (int64_t)h * G;
+    for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
+        const int g = idx / D, d = idx - g * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < W; ++w) M = fmaxf(M, cw[w * WSTRIDE + MOFF + g]);
+        float Lsum = 0.f, A = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            const float c = ex2(cw[w * WSTRIDE + MOFF + g] - M);
+            Lsum = fmaf(cw[w * WSTRIDE + LOFF + g], c, Lsum);
+            A = fmaf(cw[w * WSTRIDE + g * D + d], c, A);
+        }
+        if (n_parts == 1) {
+            p.out[(qh0 + g) * D + d] = A / Lsum;
+        } else {
+            const int64_t wi = (qh0 + g) * p.max_parts + part;
+            p.ws_acc[wi * D + d] = A;
+            if (d == 0) {
+                p.ws_m[wi] = M;
+                p.ws_l[wi] = Lsum;
+            }
+        }
+    }
+}
+
+// Merge of split-KV partials (P1 §4): M = max m_p, L = sum l_p 2^(m_p - M),
+// out = sum acc_p 2^(m_p - M) / L.  One CTA per (sequence, q-head), one
+// thread per output element.
+__global__ void decode_merge_kernel(const DecodeParams p, int D) {
+    const int s = blockIdx.x / p.num_q_heads;
+    const int g = blockIdx.x - s * p.num_q_heads;
+    const int n = __ldg(p.context_lens + s);
+    if (n <= 0) return;
+    const int n_chunks = (n + kChunk - 1) / kChunk;
+    const int n_parts = min((n_chunks + p.part_chunks - 1) / p.part_chunks, p.max_parts);
+    if (n_parts <= 1) return;
+    const int64_t base = ((int64_t)s * p.num_q_heads + g) * p.max_parts;
+    float M = -INFINITY;
+    for (int i = 0; i < n_parts; ++i) M = fmaxf(M, p.ws_m[base + i]);
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        float Lsum = 0.f, A = 0.f;
+        for (int i = 0; i < n_parts; ++i) {
+            const float c = ex2(p.ws_m[base + i] - M);
+            Lsum = fmaf(p.ws_l[base + i], c, Lsum);
+            A = fmaf(p.ws_acc[(base + i) * D + d], c, A);
+        }
+        p.out[((int64_t)s * p.num_q_heads + g) * D + d] = A / Lsum;
+    }
+}
+
+// ---------------------------------------------------------------- host side
+constexpr int kWarps = 4;
+constexpr int kStages = 3;
+constexpr int kCtasPerSm = 2;
+constexpr int kWaves = 6;
+
+struct Plan {
+    int32_t part_chunks;
+    int32_t max_parts;
+    size_t ws_bytes;
+    size_t off_l, off_acc;
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static pa_status make_plan(const pa_kv_pool* pool, int32_t B, int32_t Hq, int32_t max_ctx,
+                           int32_t partition_tokens, Plan* plan) {
+    if (B < 0 || Hq <= 0 || max_ctx < 0) return PA_ERR_INVALID_ARG;
+    const int64_t chunks_max = ((int64_t)max_ctx + kChunk - 1) / kChunk;
+    int64_t pc;
+    if (partition_tokens > 0) {
+        if (partition_tokens % kChunk != 0) return PA_ERR_INVALID_ARG;
+        pc = partition_tokens / kChunk;
+    } else if (partition_tokens == 0) {
+        const int64_t units = (int64_t)B * pool->num_kv_heads;
+        const int64_t target = (int64_t)device_sm_count() * kCtasPerSm * kWaves;
+        pc = (units * chunks_max + target - 1) / (target > 0 ? target : 1);
+        if (pc < 2 * kWarps) pc = 2 * kWarps;
+        pc = (pc + kWarps - 1) / kWarps * kWarps;
+    } else {
+        return PA_ERR_INVALID_ARG;
+    }
+    if (chunks_max > 0 && (chunks_max + pc - 1) / pc > 65535) pc = (chunks_max + 65534) / 65535;
+    if (pc > (int64_t)1 << 26) pc = (int64_t)1 << 26;
+    plan->part_chunks = (int32_t)pc;
+    plan->max_parts = (int32_t)(chunks_max > 0 ? (chunks_max + pc - 1) / pc : 1);
+    if (plan->max_parts <= 1) {
+        plan->ws_bytes = plan->off_l = plan->off_acc = 0;
+        return PA_OK;
+    }
+    const size_t rows = (size_t)B * Hq * plan->max_parts;
+    plan->off_l = align256(rows * 4);
+    plan->off_acc = plan->off_l + align256(rows * 4);
+    plan->ws_bytes = plan->off_acc + rows * (size_t)pool->head_dim * 4;
+    return PA_OK;
+}
+
+template <typename T, int G>
+static pa_status launch_partial(const DecodeParams& prm, int32_t B, int32_t Hkv, int32_t max_parts,
+                                cudaStream_t stream) {
+    using Lay = DecodeSmem<kWarps, kStages, G>;
+    auto kern = decode_partition_kernel<T, G, kWarps, kStages>;
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)Lay::total);
+        if (e != cudaSuccess) {
+            record_cuda_error(e);
+            return PA_ERR_CUDA;
+        }
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    dim3 grid((unsigned)B, (unsigned)Hkv, (unsigned)max_parts);
+    kern<<<grid, kWarps * 32, Lay::total, stream>>>(prm);
+    return launch_status();
+}
+
+template <typename T>
+static pa_status dispatch_group(int G, const DecodeParams& prm, int32_t B, int32_t Hkv,
+                                int32_t max_parts, cudaStream_t st) {
+    switch (G) {
+        case 1: return launch_partial<T, 1>(prm, B, Hkv, max_parts, st);
+        case 2: return launch_partial<T, 2>(prm, B, Hkv, max_parts, st);
+        case 4: return launch_partial<T, 4>(prm, B, Hkv, max_parts, st);
+        case 8: return launch_partial<T, 8>(prm, B, Hkv, max_parts, st);
+        default: return PA_ERR_UNSUPPORTED;
+    }
+}
+
+static void bind_workspace(const Plan& plan, void* workspace, DecodeParams* prm) {
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    prm->ws_m = plan.ws_bytes ? reinterpret_cast<float*>(ws) : nullptr;
+    prm->ws_l = plan.ws_bytes ? reinterpret_cast<float*>(ws + plan.off_l) : nullptr;
+    prm->ws_acc = plan.ws_bytes ? reinterpret_cast<float*>(ws + plan.off_acc) : nullptr;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" pa_status pa_decode_partition_tokens(const pa_kv_pool* pool, int32_t num_seqs,
+                                                int32_t num_q_heads, int32_t max_context,
+                                                int32_t* partition_tokens) {
+    pa_status st = check_pool(pool);
+    if (st != PA_OK) return st;
+    if (!partition_tokens) return PA_ERR_INVALID_ARG;
+    Plan plan;
+    st = make_plan(pool, num_seqs, num_q_heads, max_context, 0, &plan);
+    if (st != PA_OK) return st;
+    *partition_tokens = plan.part_chunks * kChunk;
+    return PA_OK;
+}
+
+extern "C" pa_status pa_decode_workspace_bytes(const pa_kv_pool* pool, int32_t num_seqs,
+                                               int32_t num_q_heads, int32_t max_context,
+                                               int32_t partition_tokens, size_t* bytes) {
+    pa_status st = check_pool(pool);
+    if (st != PA_OK) return st;
+    if (!bytes) return PA_ERR_INVALID_ARG;
+    Plan plan;
+    st = make_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan);
+    if (st != PA_OK) return st;
+    *bytes = plan.ws_bytes;
+    return PA_OK;
+}
+
+extern "C" pa_status pa_decode_partial(const pa_kv_pool* pool, const void* q,
+                                       int32_t num_q_heads, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                       int32_t num_seqs, int32_t max_context, float scale,
+                                       int32_t partition_tokens, float* out, void* workspace,
+                                       size_t workspace_bytes, int32_t* d_err,
+                                       pa_stream_t stream) {
+    pa_status st = check_pool(pool);
+    if (st != PA_OK) return st;
+    if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq < 0 || max_context < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!q || !block_tables || !context_lens || !out) return PA_ERR_INVALID_ARG;
+    if (num_q_heads % pool->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return PA_ERR_INVALID_ARG;
+    const int G = num_q_heads / pool->num_kv_heads;
+    if ((int64_t)pool->head_dim * dtype_bytes(pool->dtype) != kRowBytes) return PA_ERR_UNSUPPORTED;
+    if (!is_pow2(pool->block_size)) return PA_ERR_UNSUPPORTED;
+    if (pool->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(pool->k_pool) || !aligned16(pool->v_pool))
+        return PA_ERR_INVALID_ARG;
+    Plan plan;
+    st = make_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan);
+    if (st != PA_OK) return st;
+    if (plan.max_parts > 65535) return PA_ERR_UNSUPPORTED;
+    if (plan.ws_bytes > 0 && (workspace == nullptr || workspace_bytes < plan.ws_bytes ||
+                              !aligned16(workspace)))
+        return PA_ERR_INVALID_ARG;
+
+    DecodeParams prm;
+    prm.k_pool = static_cast<const unsigned char*>(pool->k_pool);
+    prm.v_pool = static_cast<const unsigned char*>(pool->v_pool);
+    prm.num_blocks = pool->num_blocks;
+    prm.log2_bp = ilog2(pool->block_size);
+    prm.num_kv_heads = pool->num_kv_heads;
+    prm.q = q;
+    prm.num_q_heads = num_q_heads;
+    prm.block_tables = block_tables;
+    prm.max_blocks = max_blocks_per_seq;
+    prm.context_lens = context_lens;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.part_chunks = plan.part_chunks;
+    prm.max_parts = plan.max_parts;
+    prm.out = out;
+    bind_workspace(plan, workspace, &prm);
+    prm.d_err = d_err;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (pool->dtype == PA_DTYPE_F32)
+        return dispatch_group<float>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
+    return dispatch_group<uint16_t>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
+}
+
+extern "C" pa_status pa_decode_merge(const pa_kv_pool* pool, int32_t num_q_heads,
+                                     const int32_t* context_lens, int32_t num_seqs,
+                                     int32_t max_context, int32_t partition_tokens, float* out,
+                                     void* workspace, size_t workspace_bytes,
+                                     pa_stream_t stream) {
+    pa_status st = check_pool(pool);
+    if (st != PA_OK) return st;
+    if (num_seqs < 0 || num_q_heads <= 0 || max_context < 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!context_lens || !out) return PA_ERR_INVALID_ARG;
+    Plan plan;
+    st = make_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan);
+    if (st != PA_OK) return st;
+    if (plan.max_parts <= 1) return PA_OK;
+    if (workspace == nullptr || workspace_bytes < plan.ws_bytes || !aligned16(workspace))
+        return PA_ERR_INVALID_ARG;
+    DecodeParams prm = {};
+    prm.num_q_heads = num_q_heads;
+    prm.context_lens = context_lens;
+    prm.part_chunks = plan.part_chunks;
+    prm.max_parts = plan.max_parts;
+    prm.out = out;
+    bind_workspace(plan, workspace, &prm);
+    const int D = pool->head_dim;
+    decode_merge_kernel<<<(unsigned)((int64_t)num_seqs * num_q_heads), D <= 128 ? 128 : 256, 0,
+                          (cudaStream_t)stream>>>(prm, D);
+    return launch_status();
+}
+
+extern "C" pa_status pa_decode(const pa_kv_pool* pool, const void* q, int32_t num_q_heads,
+                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, int32_t num_seqs, int32_t max_context,
+                               float scale, int32_t partition_tokens, float* out, void* workspace,
+                               size_t workspace_bytes, int32_t* d_err, pa_stream_t stream) {
+    pa_status st = pa_decode_partial(pool, q, num_q_heads, block_tables, max_blocks_per_seq,
+                                     context_lens, num_seqs, max_context, scale, partition_tokens,
+                                     out, workspace, workspace_bytes, d_err, stream);
+    if (st != PA_OK) return st;
+    return pa_decode_merge(pool, num_q_heads, context_lens, num_seqs, max_context,
+                           partition_tokens, out, workspace, workspace_bytes, stream);
+}

@@ -1,0 +1,47 @@
+// Host-side helpers shared by the entry points of libpagedkv.so.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/pagedkv.h"
+
+namespace pa {
+
+// Last CUDA error text seen by this library on the calling thread.
+void record_cuda_error(cudaError_t e);
+
+inline int32_t dtype_bytes(int32_t dtype) { return dtype == PA_DTYPE_F32 ? 4 : 2; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+inline int ilog2(int64_t x) {
+    int l = 0;
+    while ((int64_t(1) << (l + 1)) <= x) ++l;
+    return l;
+}
+
+inline pa_status check_pool(const pa_kv_pool* p) {
+    if (p == nullptr || p->k_pool == nullptr || p->v_pool == nullptr) return PA_ERR_INVALID_ARG;
+    if (p->num_blocks <= 0 || p->block_size <= 0 || p->num_kv_heads <= 0 || p->head_dim <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (p->dtype != PA_DTYPE_F32 && p->dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+// Status of the launch just made (cudaGetLastError).
+inline pa_status launch_status() {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+// Streaming multiprocessors of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace pa

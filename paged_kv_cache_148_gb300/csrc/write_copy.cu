@@ -1,0 +1,120 @@
+// pa_write_kv and pa_copy_blocks: the scatter write of new K/V rows through
+// slot_mapping (P1 §4.1 of "03｜PagedAttention 与 KV Cache 内存系统") and the
+// whole-block copy used for copy-on-write of a shared tail block (P1 §5;
+// "KV Cache：容量、布局与生命周期", section 引用计数与尾块 COW).
+//
+// Both are pure HBM copies.  Each thread moves 16-byte vectors, consecutive
+// threads touch consecutive vectors of one row or page, so every warp access
+// is a fully used 512-byte span on both the read and the write side.
+#include "common.cuh"
+#include "host_common.h"
+
+namespace pa {
+
+// One thread per 16-byte vector of a (token, kv-head) row, K and V together.
+__global__ void __launch_bounds__(256) write_kv_kernel(
+    uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, const uint4* __restrict__ k_new,
+    const uint4* __restrict__ v_new, const int64_t* __restrict__ slot_mapping, int64_t total_vecs,
+    int32_t row_vecs, int32_t num_kv_heads, int32_t block_size, int64_t num_slots,
+    int32_t* d_err) {
+    const int64_t per_token = (int64_t)row_vecs * num_kv_heads;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total_vecs;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / per_token;
+        const int64_t r = i - t * per_token;          // h * row_vecs + vec
+        const int64_t slot = __ldg(slot_mapping + t);
+        if (slot < 0 || slot >= num_slots) {
+            if (r == 0) set_error(d_err, PA_ERR_OUT_OF_RANGE);
+            continue;
+        }
+        const int64_t blk = slot / block_size, off = slot - blk * block_size;
+        const int64_t h = r / row_vecs, vec = r - h * row_vecs;
+        const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * row_vecs + vec;
+        const uint4 kx = __ldg(k_new + i);
+        const uint4 vx = __ldg(v_new + i);
+        k_pool[dst] = kx;
+        v_pool[dst] = vx;
+    }
+}
+
+// grid.x = pair, grid.y = slices of the page; each thread copies vectors of
+// the page with a stride of the slice width.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(
+    uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, const int32_t* __restrict__ src,
+    const int32_t* __restrict__ dst, int64_t page_vecs, int32_t num_blocks, int32_t* d_err) {
+    const int32_t s = __ldg(src + blockIdx.x), d = __ldg(dst + blockIdx.x);
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+        if (blockIdx.y == 0 && threadIdx.x == 0) set_error(d_err, PA_ERR_OUT_OF_RANGE);
+        return;
+    }
+    const uint4* ks = k_pool + (int64_t)s * page_vecs;
+    const uint4* vs = v_pool + (int64_t)s * page_vecs;
+    uint4* kd = k_pool + (int64_t)d * page_vecs;
+    uint4* vd = v_pool + (int64_t)d * page_vecs;
+    const int64_t step = (int64_t)gridDim.y * blockDim.x;
+    int64_t v = (int64_t)blockIdx.y * blockDim.x + threadIdx.x;
+    // two vectors of K and two of V in flight per iteration
+    for (; v + step < page_vecs; v += 2 * step) {
+        const uint4 a = ks[v], b = ks[v + step], c = vs[v], e = vs[v + step];
+        kd[v] = a;
+        kd[v + step] = b;
+        vd[v] = c;
+        vd[v + step] = e;
+    }
+    if (v < page_vecs) {
+        kd[v] = ks[v];
+        vd[v] = vs[v];
+    }
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" pa_status pa_write_kv(const pa_kv_pool* pool, const void* k_new, const void* v_new,
+                                 const int64_t* slot_mapping, int32_t num_tokens, int32_t* d_err,
+                                 pa_stream_t stream) {
+    pa_status st = check_pool(pool);
+    if (st != PA_OK) return st;
+    if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping) return PA_ERR_INVALID_ARG;
+    const int64_t row_bytes = (int64_t)pool->head_dim * dtype_bytes(pool->dtype);
+    if (row_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(pool->k_pool) ||
+        !aligned16(pool->v_pool))
+        return PA_ERR_INVALID_ARG;
+    const int32_t row_vecs = (int32_t)(row_bytes / 16);
+    const int64_t total = (int64_t)num_tokens * pool->num_kv_heads * row_vecs;
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    if (blocks > 1048576) blocks = 1048576;
+    write_kv_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
+        (uint4*)pool->k_pool, (uint4*)pool->v_pool, (const uint4*)k_new, (const uint4*)v_new,
+        slot_mapping, total, row_vecs, pool->num_kv_heads, pool->block_size,
+        (int64_t)pool->num_blocks * pool->block_size, d_err);
+    return launch_status();
+}
+
+extern "C" pa_status pa_copy_blocks(const pa_kv_pool* pool, const int32_t* src,
+                                    const int32_t* dst, int32_t n, int32_t* d_err,
+                                    pa_stream_t stream) {
+    pa_status st = check_pool(pool);
+    if (st != PA_OK) return st;
+    if (n < 0) return PA_ERR_INVALID_ARG;
+    if (n == 0) return PA_OK;
+    if (!src || !dst) return PA_ERR_INVALID_ARG;
+    const int64_t page_bytes = (int64_t)pool->num_kv_heads * pool->block_size * pool->head_dim *
+                               dtype_bytes(pool->dtype);
+    if (page_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(pool->k_pool) || !aligned16(pool->v_pool)) return PA_ERR_INVALID_ARG;
+    const int64_t page_vecs = page_bytes / 16;
+    const int threads = 256;
+    int64_t slices = (page_vecs + threads * 4 - 1) / (threads * 4);
+    if (slices < 1) slices = 1;
+    if (slices > 65535) slices = 65535;
+    dim3 grid((unsigned)n, (unsigned)slices);
+    copy_blocks_kernel<<<grid, threads, 0, (cudaStream_t)stream>>>(
+        (uint4*)pool->k_pool, (uint4*)pool->v_pool, src, dst, page_vecs, pool->num_blocks, d_err);
+    return launch_status();
+}
