@@ -249,6 +249,22 @@ def reference_steps(wl, warmup: int, steps: int, budget_s: float):
                       % (wl.num_q_heads, done, el)}
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The slowest rank's time (one all-reduce, outside any timed region)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(bytes_per_rank: int, world: int, max_ms: float) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's step time."""
+    return world * bytes_per_rank / (max_ms * 1e-3) / 1e9
+
+
 # --------------------------------------------------------------------------- GPU arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -311,11 +327,7 @@ def run_ours(args, rank, world, local_rank):
     write_ms = np.array([e[0].elapsed_time(e[1]) for e in ev])
     attn_ms = np.array([e[1].elapsed_time(e[2]) for e in ev])
     merge_ms = np.array([e[2].elapsed_time(e[3]) for e in ev])
-    ms = float(step_ms.mean())
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(float(step_ms.mean()), world, dev)
 
     # end-to-end through the public API with host buffers
     e2e = run_e2e(args, g, stream, dev, is_decode)
@@ -336,7 +348,7 @@ def run_ours(args, rank, world, local_rank):
            "split_kv_partitions_max": max_parts}
     if is_decode:
         per_rank = ab["decode_total"]
-        res.update({"value": world * per_rank / (ms * 1e-3) / 1e9, "unit": "GB/s",
+        res.update({"value": aggregate_value(per_rank, world, ms), "unit": "GB/s",
                     "higher_is_better": True,
                     "tokens_per_s": world * wl.num_seqs / (ms * 1e-3),
                     "pct_of_hbm_peak": 100.0 * (per_rank / (ms * 1e-3) / 1e9) / hbm_peak,

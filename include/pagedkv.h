@@ -218,20 +218,25 @@ pa_status pa_decode_merge(const pa_kv_pool* pool, int32_t num_q_heads,
  * including those new ones (already written with pa_write_kv); new token i
  * sits at position context_lens[s] - n_new + i.  With causal != 0 it attends
  * to positions 0..its own; otherwise to all context_lens[s] positions.
- *   q:            device bf16 [total_q][num_q_heads][head_dim].
+ *   q:            device bf16 [total_q][num_q_heads][head_dim];
+ *                 total_q = cu_seqlens_q[num_seqs] (bounds the tiled loads).
  *   cu_seqlens_q: device int32 [num_seqs + 1].
  *   context_lens: device int32 [num_seqs].
  *   block_tables: device int32 [num_seqs][max_blocks_per_seq].
- *   max_q_len, max_context: host upper bounds (size the grid).
+ *   max_q_len:    host upper bound of the per-sequence query counts (grid).
+ *   max_context:  host upper bound of context_lens.
  *   out:          device float32 [total_q][num_q_heads][head_dim].
  * Implemented: bf16, head_dim 128, block size a power of two in [8, 128],
  * num_q_heads / num_kv_heads in {1, 2, 4, 8}, pool and q 16-byte aligned.
+ * A table entry outside the pool is read as block 0 and sets *d_err; a
+ * sequence with context_lens < its query count sets PA_ERR_INVALID_ARG.
  */
-pa_status pa_prefill(const pa_kv_pool* pool, const void* q, int32_t num_q_heads,
-                     const int32_t* cu_seqlens_q, const int32_t* context_lens,
-                     const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t num_seqs,
-                     int32_t max_q_len, int32_t max_context, float scale, int32_t causal,
-                     float* out, int32_t* d_err, pa_stream_t stream);
+pa_status pa_prefill(const pa_kv_pool* pool, const void* q, int32_t total_q,
+                     int32_t num_q_heads, const int32_t* cu_seqlens_q,
+                     const int32_t* context_lens, const int32_t* block_tables,
+                     int32_t max_blocks_per_seq, int32_t num_seqs, int32_t max_q_len,
+                     int32_t max_context, float scale, int32_t causal, float* out,
+                     int32_t* d_err, pa_stream_t stream);
 
 /*
  * Host block allocator: refcounts, free list, fork and copy-on-write tail

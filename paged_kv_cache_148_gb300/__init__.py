@@ -94,7 +94,7 @@ def lib() -> ctypes.CDLL:
         "pa_decode": ([P, P, i32, P, i32, P, i32, i32, f32, i32, P, P, sz, P, P], i32),
         "pa_decode_partial": ([P, P, i32, P, i32, P, i32, i32, f32, i32, P, P, sz, P, P], i32),
         "pa_decode_merge": ([P, i32, P, i32, i32, i32, P, P, sz, P], i32),
-        "pa_prefill": ([P, P, i32, P, P, P, i32, i32, i32, i32, f32, i32, P, P, P], i32),
+        "pa_prefill": ([P, P, i32, i32, P, P, P, i32, i32, i32, i32, f32, i32, P, P, P], i32),
         "pa_alloc_create": ([i32, P, P], i32),
         "pa_alloc_destroy": ([P], None),
         "pa_alloc_append": ([P, P, P, i32], i32),
@@ -292,7 +292,7 @@ def prefill(pool: KVPool, q: torch.Tensor, cu_seqlens_q: torch.Tensor, context_l
     if out is None:
         out = torch.empty((T, Hq, D), dtype=torch.float32, device=pool.device)
     _need(out, "out", torch.float32, pool.device)
-    _check(lib().pa_prefill(pool.c, _ptr(q), Hq, _ptr(cu_seqlens_q), _ptr(context_lens),
+    _check(lib().pa_prefill(pool.c, _ptr(q), T, Hq, _ptr(cu_seqlens_q), _ptr(context_lens),
                             _ptr(block_tables), int(block_tables.shape[1]),
                             int(context_lens.shape[0]), int(max_q_len), int(max_context),
                             float(scale), 1 if causal else 0, _ptr(out), _ptr(d_err),

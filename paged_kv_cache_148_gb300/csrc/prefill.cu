@@ -1,15 +1,497 @@
-// pa_prefill: paged chunked-prefill attention (tensor-core kernel pending).
+// pa_prefill: paged chunked-prefill attention on the 5th-generation tensor
+// cores (tcgen05, accumulators in TMEM, operands staged by TMA).
+//
+// Semantics: "03｜PagedAttention 与 KV Cache 内存系统" §4 — prefill reuses a
+// flash-style tiled attention kernel that is handed the paged block table
+// (paging decides where K/V live, tiling decides how one attention pass moves
+// through them).  New token i of a sequence sits at position
+// context_len - n_new + i and, with a causal mask, sees positions 0..itself.
+//
+// CTA = (q-tile, kv-head, sequence).  A tile is 128 rows = (128/G) queries x
+// the G query heads that share one kv-head, so every K/V byte staged in
+// shared memory feeds all G heads.  Key tiles are 128 keys = 128/B_p pages,
+// each page half (64 dims) fetched by one tiled TMA load straight from the
+// pool through the block table.
+//
+// Roles (192 threads):
+//   warp 0  TMA producer: Q tile once, then K/V tiles into a 2-stage ring.
+//   warp 1  MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
+//           buffers, then O += P_{j-1} V_{j-1} once the softmax published
+//           P_{j-1}; tcgen05.commit signals completion on mbarriers.
+//   warps 2-5  softmax: thread r owns row r (TMEM lane r): loads S_j, masks,
+//           online softmax in base 2 with lazy rescaling of O (only when the
+//           row max grows by more than 2^8), writes P_j as bf16 into a
+//           128-byte-swizzled K-major tile, and finally normalises O.
+// All mbarrier waits are bounded; a wait that runs out sets PA_ERR_TIMEOUT
+// and the CTA winds down.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <mutex>
+
 #include "common.cuh"
 #include "host_common.h"
+#include "tcgen05.cuh"
 
-extern "C" pa_status pa_prefill(const pa_kv_pool* pool, const void* q, int32_t num_q_heads,
-                                const int32_t* cu_seqlens_q, const int32_t* context_lens,
-                                const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                int32_t num_seqs, int32_t max_q_len, int32_t max_context,
-                                float scale, int32_t causal, float* out, int32_t* d_err,
-                                pa_stream_t stream) {
-    (void)pool; (void)q; (void)num_q_heads; (void)cu_seqlens_q; (void)context_lens;
-    (void)block_tables; (void)max_blocks_per_seq; (void)num_seqs; (void)max_q_len;
-    (void)max_context; (void)scale; (void)causal; (void)out; (void)d_err; (void)stream;
-    return PA_ERR_UNSUPPORTED;
+namespace pa {
+
+constexpr int kPfRows = 128;            // M: rows of a tile (queries x heads)
+constexpr int kPfKeys = 128;            // N: keys per KV tile
+constexpr int kPfDim = 128;             // head_dim
+constexpr int kHalf = 128 * 128;        // bytes of one 64-column half of a 128-row bf16 tile
+constexpr int kTile = 2 * kHalf;        // 32 KiB
+constexpr int kPfThreads = 192;
+constexpr uint32_t kTmemCols = 512;     // S0 | S1 | O (| unused)
+constexpr float kPfRescale = 8.0f;
+
+// shared-memory map (offsets from a 1024-aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffK = kTile;            // 2 stages
+constexpr int kOffV = 3 * kTile;        // 2 stages
+constexpr int kOffP = 5 * kTile;
+constexpr int kOffBar = 6 * kTile;
+constexpr int kPfSmem = kOffBar + 256 + 1024;  // + barriers, + alignment slack
+
+struct PrefillParams {
+    const int32_t* cu_seqlens_q;
+    const int32_t* context_lens;
+    const int32_t* block_tables;
+    int32_t max_blocks;
+    int32_t num_blocks;
+    int32_t num_kv_heads;
+    int32_t num_q_heads;
+    int32_t log2_bp;
+    int32_t causal;
+    float scale_log2;
+    int32_t max_qtiles;
+    float* out;
+    int32_t* d_err;
+};
+
+struct PfBars {
+    uint64_t q_full;
+    uint64_t kv_full[2];
+    uint64_t kv_empty[2];
+    uint64_t s_full[2];
+    uint64_t s_empty[2];
+    uint64_t p_full;
+    uint64_t o_done;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+
+PA_DEVICE uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+PA_DEVICE void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// bounded wait that also honours a CTA-wide abort flag
+PA_DEVICE bool pf_wait(uint64_t* bar, uint32_t parity, PfBars* b, int32_t* d_err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t spins = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if ((++spins & 255u) == 0) {
+            if (*(volatile int32_t*)&b->abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                set_error(d_err, PA_ERR_TIMEOUT);
+                *(volatile int32_t*)&b->abort = 1;
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kPfThreads, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+               const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
+    constexpr int QT = kPfRows / G;  // queries per tile
+    const int qt = p.max_qtiles - 1 - (int)blockIdx.x;  // longest tiles first
+    const int h = blockIdx.y, s = blockIdx.z;
+    const int q_begin = __ldg(p.cu_seqlens_q + s);
+    const int n_new = __ldg(p.cu_seqlens_q + s + 1) - q_begin;
+    const int q0 = qt * QT;
+    if (n_new <= 0 || q0 >= n_new) {
+        if (qt == 0 && h == 0 && threadIdx.x == 0 && n_new > p.max_qtiles * QT)
+            set_error(p.d_err, PA_ERR_OUT_OF_RANGE);
+        return;
+    }
+    const int ctx = __ldg(p.context_lens + s);
+    const int base_pos = ctx - n_new;  // position of new token 0
+    if (base_pos < 0) {
+        if (threadIdx.x == 0) set_error(p.d_err, PA_ERR_INVALID_ARG);
+        return;
+    }
+    const int q_last = min(q0 + QT, n_new) - 1;
+    const int kv_end = p.causal ? base_pos + q_last + 1 : ctx;  // keys [0, kv_end)
+    const int n_tiles = (kv_end + kPfKeys - 1) / kPfKeys;
+    const int bp = 1 << p.log2_bp;
+    const int pages_per_tile = kPfKeys >> p.log2_bp;
+    // keys at or past `zlim` may be unwritten or not loaded: V rows there are zeroed
+    const int zlim = min(ctx, ((kv_end + bp - 1) >> p.log2_bp) << p.log2_bp);
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PfBars* bars = reinterpret_cast<PfBars*>(smem + kOffBar);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->kv_full[i], 1);
+            mbar_init(&bars->kv_empty[i], 1);
+            mbar_init(&bars->s_full[i], 1);
+            mbar_init(&bars->s_empty[i], 128);
+        }
+        mbar_init(&bars->p_full, 128);
+        mbar_init(&bars->o_done, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&bars->tmem_base, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t tS = tmem;             // columns [0, 256): two S buffers
+    const uint32_t tO = tmem + 256;       // columns [256, 384): O
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tc::prefetch_tmap(&tmap_q);
+            tc::prefetch_tmap(&tmap_k);
+            tc::prefetch_tmap(&tmap_v);
+            mbar_arrive_expect_tx(&bars->q_full, kTile);
+            tc::tma_load_3d(smem + kOffQ, &tmap_q, 0, h * G, q_begin + q0, &bars->q_full);
+            tc::tma_load_3d(smem + kOffQ + kHalf, &tmap_q, 64, h * G, q_begin + q0, &bars->q_full);
+            const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !pf_wait(&bars->kv_empty[st], ((j >> 1) - 1) & 1, bars, p.d_err)) break;
+                const int e0 = j * pages_per_tile;
+                int loaded = 0;
+                for (int k = 0; k < pages_per_tile; ++k)
+                    if (((e0 + k) << p.log2_bp) < kv_end) ++loaded;
+                mbar_arrive_expect_tx(&bars->kv_full[st], (uint32_t)loaded * bp * 128 * 2 * 2);
+                unsigned char* kst = smem + kOffK + st * kTile;
+                unsigned char* vst = smem + kOffV + st * kTile;
+                for (int k = 0; k < loaded; ++k) {
+                    const int e = e0 + k;
+                    int32_t id = e < p.max_blocks ? __ldg(table + e) : -1;
+                    if (id < 0 || id >= p.num_blocks) {
+                        set_error(p.d_err, id < 0 ? PA_ERR_NEGATIVE_BLOCK : PA_ERR_OUT_OF_RANGE);
+                        id = 0;  // stay in bounds; the result is flagged as invalid
+                    }
+                    const int row = (id * p.num_kv_heads + h) << p.log2_bp;
+                    const int off = k * bp * 128;
+                    tc::tma_load_2d(kst + off, &tmap_k, 0, row, &bars->kv_full[st]);
+                    tc::tma_load_2d(kst + kHalf + off, &tmap_k, 64, row, &bars->kv_full[st]);
+                    tc::tma_load_2d(vst + off, &tmap_v, 0, row, &bars->kv_full[st]);
+                    tc::tma_load_2d(vst + kHalf + off, &tmap_v, 64, row, &bars->kv_full[st]);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, 128, 0, 0);
+            constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, 128, 0, 1);
+            const uint32_t q_addr = smem_u32(smem + kOffQ);
+            const uint32_t p_addr = smem_u32(smem + kOffP);
+            bool ok = pf_wait(&bars->q_full, 0, bars, p.d_err);
+            auto pv = [&](int t) -> bool {
+                if (!pf_wait(&bars->p_full, t & 1, bars, p.d_err)) return false;
+                tc::fence_after_sync();
+                const uint32_t v_addr = smem_u32(smem + kOffV + (t & 1) * kTile);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t a = tc::smem_desc_sw128(p_addr + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = tc::smem_desc_sw128(v_addr + kk * 2048, kHalf, 1024);
+                    tc::mma_bf16(tO, a, b, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::commit(&bars->o_done);
+                tc::commit(&bars->kv_empty[t & 1]);
+                return true;
+            };
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int st = j & 1;
+                if (!pf_wait(&bars->kv_full[st], (j >> 1) & 1, bars, p.d_err)) { ok = false; break; }
+                if (j >= 2 && !pf_wait(&bars->s_empty[st], ((j >> 1) - 1) & 1, bars, p.d_err)) { ok = false; break; }
+                tc::fence_after_sync();
+                const uint32_t k_addr = smem_u32(smem + kOffK + st * kTile);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    const uint64_t a = tc::smem_desc_sw128(q_addr + koff, 16, 1024);
+                    const uint64_t b = tc::smem_desc_sw128(k_addr + koff, 16, 1024);
+                    tc::mma_bf16(tS + st * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+                }
+                tc::commit(&bars->s_full[st]);
+                if (j >= 1 && !pv(j - 1)) { ok = false; break; }
+            }
+            if (ok) pv(n_tiles - 1);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;        // tile row == TMEM lane
+        const int i = r / G, g = r - i * G;
+        const int qi = q0 + i;
+        const bool live = qi < n_new;
+        int lim = p.causal ? base_pos + qi : ctx - 1;  // last visible key
+        if (!live) lim = 0;
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        const uint32_t p_row = smem_u32(smem + kOffP) + r * 128;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int sb = j & 1;
+            ok = pf_wait(&bars->s_full[sb], (j >> 1) & 1, bars, p.d_err);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc::fence_after_sync();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc::tmem_ld32(tS + lane_addr + sb * 128 + c * 32, sr[c]);
+            tc::tmem_wait_ld();
+            tc::fence_before_sync();
+            mbar_arrive(&bars->s_empty[sb]);
+
+            const int key0 = j * kPfKeys;
+            float tmax = -INFINITY;
+            const bool full = key0 + kPfKeys - 1 <= lim;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    float x = __uint_as_float(sr[c][e]) * p.scale_log2;
+                    if (!full && key0 + c * 32 + e > lim) x = -INFINITY;
+                    sr[c][e] = __float_as_uint(x);
+                    tmax = fmaxf(tmax, x);
+                }
+            bool o_ready = false;
+            if (j == 0) {
+                m_used = tmax;
+            } else {
+                const float m_new = fmaxf(m_used, tmax);
+                const bool need = m_new > m_used + kPfRescale;
+                if (__any_sync(0xffffffffu, need)) {
+                    // O holds tiles < j at scale m_used: wait for PV_{j-1}, then rescale
+                    ok = pf_wait(&bars->o_done, (j - 1) & 1, bars, p.d_err);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    o_ready = true;
+                    tc::fence_after_sync();
+                    const float f = need ? ex2(m_used - m_new) : 1.f;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tc::tmem_ld32(tO + lane_addr + c * 32, o);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                        tc::tmem_st32(tO + lane_addr + c * 32, o);
+                    }
+                    tc::tmem_wait_st();
+                    tc::fence_before_sync();
+                    l *= f;
+                    if (need) m_used = m_new;
+                }
+            }
+            // probabilities (masked keys give exactly 0)
+            float lsum = 0.f;
+            uint32_t pk[64];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float a = ex2(__uint_as_float(sr[c][e]) - m_used);
+                    const float b2 = ex2(__uint_as_float(sr[c][e + 1]) - m_used);
+                    const uint32_t w = pack_bf16(a, b2);
+                    // the row sum uses the rounded weights the tensor cores see
+                    lsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+                    pk[(c * 32 + e) >> 1] = w;
+                }
+            l += lsum;
+            // the P tile is single-buffered: PV_{j-1} must have finished reading it
+            if (j >= 1 && !o_ready) {
+                ok = pf_wait(&bars->o_done, (j - 1) & 1, bars, p.d_err);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            }
+            if (key0 + kPfKeys > zlim) {
+                // last tile: V rows past the written/loaded keys may hold NaN; zero them
+                ok = pf_wait(&bars->kv_full[sb], (j >> 1) & 1, bars, p.d_err);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                if (key0 + r >= zlim) {
+                    const uint32_t vrow = smem_u32(smem + kOffV + sb * kTile) + r * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        st_shared_v4(vrow + c * 16, 0, 0, 0, 0);
+                        st_shared_v4(vrow + kHalf + c * 16, 0, 0, 0, 0);
+                    }
+                }
+            }
+            // P row r: 16-byte chunk c (keys 8c..8c+7) at chunk (c mod 8) ^ (r mod 8) of half c/8
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const uint32_t addr = p_row + (c >> 3) * kHalf + (((c & 7) ^ (r & 7)) << 4);
+                st_shared_v4(addr, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->p_full);
+        }
+        // epilogue: O / l -> out
+        if (ok) ok = pf_wait(&bars->o_done, (n_tiles - 1) & 1, bars, p.d_err);
+        if (__all_sync(0xffffffffu, ok)) {
+            tc::fence_after_sync();
+            const float inv = live ? 1.f / l : 0.f;
+            float* orow = p.out + ((int64_t)(q_begin + qi) * p.num_q_heads + h * G + g) * kPfDim;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[32];
+                tc::tmem_ld32(tO + lane_addr + c * 32, o);
+                tc::tmem_wait_ld();
+                if (live) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(orow + c * 32 + e) =
+                            make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                                        __uint_as_float(o[e + 2]) * inv,
+                                        __uint_as_float(o[e + 3]) * inv);
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                     const cuuint64_t* strides, const cuuint32_t* box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int G>
+static pa_status launch_prefill(const pa_kv_pool* pool, const void* q, int32_t total_q,
+                                int32_t Hq, int32_t B, const PrefillParams& prm,
+                                cudaStream_t stream) {
+    constexpr int QT = kPfRows / G;
+    CUtensorMap mq, mk, mv;
+    const cuuint64_t qdims[3] = {(cuuint64_t)kPfDim, (cuuint64_t)Hq, (cuuint64_t)total_q};
+    const cuuint64_t qstr[2] = {(cuuint64_t)kPfDim * 2, (cuuint64_t)Hq * kPfDim * 2};
+    const cuuint32_t qbox[3] = {64, (cuuint32_t)G, (cuuint32_t)QT};
+    const cuuint64_t rows = (cuuint64_t)pool->num_blocks * pool->num_kv_heads * pool->block_size;
+    const cuuint64_t kdims[2] = {(cuuint64_t)kPfDim, rows};
+    const cuuint64_t kstr[1] = {(cuuint64_t)kPfDim * 2};
+    const cuuint32_t kbox[2] = {64, (cuuint32_t)pool->block_size};
+    if (!make_map(&mq, q, 3, qdims, qstr, qbox) || !make_map(&mk, pool->k_pool, 2, kdims, kstr, kbox) ||
+        !make_map(&mv, pool->v_pool, 2, kdims, kstr, kbox))
+        return PA_ERR_CUDA;
+    auto kern = prefill_kernel<G>;
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+        if (e != cudaSuccess) {
+            record_cuda_error(e);
+            return PA_ERR_CUDA;
+        }
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    dim3 grid((unsigned)prm.max_qtiles, (unsigned)pool->num_kv_heads, (unsigned)B);
+    kern<<<grid, kPfThreads, kPfSmem, stream>>>(mq, mk, mv, prm);
+    return launch_status();
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" pa_status pa_prefill(const pa_kv_pool* pool, const void* q, int32_t total_q,
+                                int32_t num_q_heads, const int32_t* cu_seqlens_q,
+                                const int32_t* context_lens, const int32_t* block_tables,
+                                int32_t max_blocks_per_seq, int32_t num_seqs, int32_t max_q_len,
+                                int32_t max_context, float scale, int32_t causal, float* out,
+                                int32_t* d_err, pa_stream_t stream) {
+    pa_status st = check_pool(pool);
+    if (st != PA_OK) return st;
+    if (num_seqs < 0 || total_q < 0 || num_q_heads <= 0 || max_q_len < 0 || max_context < 0 ||
+        max_blocks_per_seq < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return PA_OK;
+    if (!q || !cu_seqlens_q || !context_lens || !block_tables || !out) return PA_ERR_INVALID_ARG;
+    if (num_q_heads % pool->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return PA_ERR_INVALID_ARG;
+    const int G = num_q_heads / pool->num_kv_heads;
+    if (pool->dtype != PA_DTYPE_BF16 || pool->head_dim != kPfDim) return PA_ERR_UNSUPPORTED;
+    if (!is_pow2(pool->block_size) || pool->block_size < 8 || pool->block_size > 128)
+        return PA_ERR_UNSUPPORTED;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
+    if (pool->num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)pool->num_blocks * pool->num_kv_heads * pool->block_size > INT32_MAX)
+        return PA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(pool->k_pool) || !aligned16(pool->v_pool))
+        return PA_ERR_INVALID_ARG;
+    PrefillParams prm;
+    prm.cu_seqlens_q = cu_seqlens_q;
+    prm.context_lens = context_lens;
+    prm.block_tables = block_tables;
+    prm.max_blocks = max_blocks_per_seq;
+    prm.num_blocks = pool->num_blocks;
+    prm.num_kv_heads = pool->num_kv_heads;
+    prm.num_q_heads = num_q_heads;
+    prm.log2_bp = ilog2(pool->block_size);
+    prm.causal = causal ? 1 : 0;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    const int QT = kPfRows / G;
+    prm.max_qtiles = (max_q_len + QT - 1) / QT;
+    prm.out = out;
+    prm.d_err = d_err;
+    cudaStream_t cs = (cudaStream_t)stream;
+    switch (G) {
+        case 1: return launch_prefill<1>(pool, q, total_q, num_q_heads, num_seqs, prm, cs);
+        case 2: return launch_prefill<2>(pool, q, total_q, num_q_heads, num_seqs, prm, cs);
+        case 4: return launch_prefill<4>(pool, q, total_q, num_q_heads, num_seqs, prm, cs);
+        default: return launch_prefill<8>(pool, q, total_q, num_q_heads, num_seqs, prm, cs);
+    }
 }

@@ -1,0 +1,82 @@
+"""CPU checks of bench.py: multi-rank aggregation (world size 2 over gloo),
+the algorithmic byte count, and the reference (oracle) arm's JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+import workloads  # noqa: E402
+
+
+def _rank_main(rank, world, port, ms_by_rank, out_q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        mx = bench.max_over_ranks(ms_by_rank[rank], world)
+        val = bench.aggregate_value(1_000_000_000, world, mx)
+        out_q.put((rank, mx, val))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + (os.getpid() % 1000)
+    ms = [0.25, 0.5]
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, ms, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, mx, val in res:
+        assert mx == 0.5                      # every rank sees the slowest rank's time
+        assert val == pytest.approx(2 * 1e9 / 0.5e-3 / 1e9)
+
+
+def test_single_rank_passthrough():
+    assert bench.max_over_ranks(1.5, 1) == 1.5
+    assert bench.aggregate_value(2_000_000_000, 1, 1.0) == pytest.approx(2000.0)
+
+
+def test_algorithmic_bytes_decode_gqa():
+    wl = workloads.decode_gqa()
+    ab = bench.algorithmic_bytes(wl)
+    n = wl.total_lens
+    assert ab["kv"] == int(n.sum()) * 2 * 8 * 128 * 2
+    assert ab["q"] == 64 * 32 * 128 * 2 and ab["out"] == 64 * 32 * 128 * 4
+    assert ab["tables"] == int(np.ceil(n / 16).sum()) * 4
+    assert ab["decode_total"] == ab["kv"] + ab["q"] + ab["out"] + ab["tables"] + ab["lens"]
+    assert 5.0e8 < ab["kv"] < 6.2e8       # about 554 MB of K/V per step
+
+
+def test_prefill_flops_matches_closed_form():
+    wl = workloads.prefill()
+    # 16 sequences, queries at positions 2048..2559 see pos+1 keys
+    vis = 16 * sum(2048 + 1 + i for i in range(512))
+    assert bench.prefill_flops(wl) == 4.0 * 128 * 32 * vis
+    assert abs(bench.prefill_flops(wl) / 1e9 - 309.3) < 0.1
+
+
+def test_reference_arm_prints_contract_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "decode_tiny", "--steps", "3", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    for k in ("metric", "value", "unit", "cpu_baseline", "e2e", "config"):
+        assert k in line
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"

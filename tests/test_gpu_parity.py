@@ -88,8 +88,9 @@ def test_write_kv_and_tables_bit_exact(name, make):
 
 
 def test_write_kv_rejects_out_of_pool_slot_and_writes_the_rest():
-    wl = workloads.decode_gqa(scale=1 / 32)
+    wl = workloads.decode_gqa(scale=1 / 8)
     g = GpuWorkload(wl)
+    assert wl.num_seqs >= 4
     before_k = _pool_bits(g.cache.pool.k).copy()
     bad = g.slot_mapping.clone()
     n_slots = wl.num_blocks * wl.block_size
@@ -113,6 +114,7 @@ def test_write_kv_rejects_out_of_pool_slot_and_writes_the_rest():
 def test_copy_blocks_bit_exact(block_size, dtype, D):
     wl = workloads.custom_decode(6, 8, 2, D, block_size, dtype, [37, 5, 64, 1, 90, 17], seed=3)
     g = GpuWorkload(wl)
+    g.write_new()
     oc = oracle.OracleCache(wl)
     rng = np.random.default_rng(4)
     held = sorted({b for t in oc.tables for b in t})
