@@ -52,6 +52,11 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--l2", choices=["none", "flush"], default="none",
+                    help="none: the step's K/V (4x the 129 MB L2) is itself larger than L2; "
+                         "flush: write a 256 MiB buffer before every timed step")
+    ap.add_argument("--partition-tokens", type=int, default=0,
+                    help="split-KV partition size for decode (0 = the library's choice)")
     return ap.parse_args()
 
 
@@ -77,6 +82,10 @@ def algorithmic_bytes(wl) -> dict:
     write = n_q * wl.num_kv_heads * wl.head_dim * e * 2 * 2 + n_q * 8
     return {"kv": kv, "q": q, "out": out, "tables": tables, "lens": lens, "write": write,
             "decode_total": kv + q + out + tables + lens}
+
+
+def ab_kv_mb(wl) -> float:
+    return algorithmic_bytes(wl)["kv"] / 1e6
 
 
 def prefill_flops(wl) -> float:
@@ -180,9 +189,10 @@ def cpu_oracle_run(wl, seconds: float):
     t_budget = seconds
     if wl.kind == "decode":
         # sequences in batch order until ~t_budget of work, measured by doing it
-        done_bytes, elapsed, s = 0, 0.0, 0
+        done_bytes, elapsed, done = 0, 0.0, 0
         per_tok = wl.logical_bytes_per_token()
-        while s < wl.num_seqs and elapsed < t_budget:
+        while done < wl.num_seqs or elapsed < t_budget:
+            s = done % wl.num_seqs
             rows = [(s, g) for g in range(wl.num_q_heads)]
             t0 = time.perf_counter()
             oracle.decode(oc.k, oc.v, q, oc.tables, wl.total_lens, wl.scale, rows=rows)
@@ -190,12 +200,13 @@ def cpu_oracle_run(wl, seconds: float):
             n = int(wl.total_lens[s])
             done_bytes += (n * per_tok + wl.num_q_heads * wl.head_dim * (wl.elem_bytes + 4)
                            + 4 * (-(-n // wl.block_size)) + 4)
-            s += 1
+            done += 1
         return {"value": done_bytes / elapsed / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
                 "kind": "oracle",
-                "sample": "float64 oracle decode of the first %d of %d sequences (all %d q-heads), "
-                          "%.1f s" % (s, wl.num_seqs, wl.num_q_heads, elapsed),
-                "seconds": elapsed, "tokens_per_s": s / elapsed}
+                "sample": "float64 oracle decode, %d sequence passes over the %d-sequence batch "
+                          "(all %d q-heads each), %.1f s" % (done, wl.num_seqs, wl.num_q_heads,
+                                                           elapsed),
+                "seconds": elapsed, "tokens_per_s": done / elapsed}
     # prefill: a sample of (token, head) rows, scaled to TFLOP/s of visible work
     cu = np.concatenate([[0], np.cumsum(wl.new_lens)])
     rng = np.random.default_rng(0)
@@ -277,6 +288,8 @@ def run_ours(args, rank, world, local_rank):
     pkv.build()
     wl = workloads.WORKLOADS[args.workload]()
     g = GpuWorkload(wl, device=dev)
+    if args.partition_tokens:
+        g.set_partition_tokens(args.partition_tokens)
     stream = torch.cuda.current_stream(dev)
     is_decode = wl.kind == "decode"
     max_parts = g.max_parts()
@@ -290,8 +303,10 @@ def run_ours(args, rank, world, local_rank):
         else:
             g.attend(stream)
 
+    do_flush = args.l2 == "flush"
     for i in range(args.warmup):
-        flush.fill_(i & 255)
+        if do_flush:
+            flush.fill_(i & 255)
         step()
     torch.cuda.synchronize(dev)
     g.err.zero_()
@@ -303,7 +318,8 @@ def run_ours(args, rank, world, local_rank):
     clocks = ClockSampler(local_rank)
     clocks.start()
     for i in range(K):
-        flush.fill_(i & 255)
+        if do_flush:
+            flush.fill_(i & 255)
         e = ev[i]
         e[0].record(stream)
         g.write_new(stream)
@@ -344,8 +360,12 @@ def run_ours(args, rank, world, local_rank):
                                                       int(wl.total_lens.min()),
                                                       int(wl.total_lens.max())),
            "per_rank": "each rank runs its own copy of the batch (independent replicas)",
-           "l2": "flushed before every timed step by a 256 MiB write outside the step's events",
-           "split_kv_partitions_max": max_parts}
+           "l2": ("flushed before every timed step by a 256 MiB write outside the step's events"
+                  if do_flush else
+                  "no flush: inputs larger than L2 (the step reads %.0f MB of K/V, L2 is 129 MB)"
+                  % (ab_kv_mb(wl))),
+           "split_kv_partitions_max": max_parts,
+           "partition_tokens": args.partition_tokens or "auto"}
     if is_decode:
         per_rank = ab["decode_total"]
         res.update({"value": aggregate_value(per_rank, world, ms), "unit": "GB/s",
@@ -416,7 +436,8 @@ def run_e2e(args, g, stream, dev, is_decode):
     n = max(1, args.e2e_steps)
     ms = []
     for i in range(n):
-        flush.fill_(i & 255)
+        if args.l2 == "flush":
+            flush.fill_(i & 255)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)

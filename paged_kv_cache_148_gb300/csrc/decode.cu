@@ -77,6 +77,10 @@ struct Row<float> {
         f[2] = __uint_as_float(u.z);
         f[3] = __uint_as_float(u.w);
     }
+    static PA_DEVICE void unpack2(const uint4& u, float2 (&f)[2]) {
+        f[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+        f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+    }
 };
 template <>
 struct Row<uint16_t> {  // bf16 bit patterns
@@ -87,6 +91,12 @@ struct Row<uint16_t> {  // bf16 bit patterns
         f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
         f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
     }
+    static PA_DEVICE void unpack2(const uint4& u, float2 (&f)[4]) {
+        f[0] = make_float2(bf16_lo(u.x), bf16_hi(u.x));
+        f[1] = make_float2(bf16_lo(u.y), bf16_hi(u.y));
+        f[2] = make_float2(bf16_lo(u.z), bf16_hi(u.z));
+        f[3] = make_float2(bf16_lo(u.w), bf16_hi(u.w));
+    }
 };
 
 template <int W, int S, int G>
@@ -95,7 +105,7 @@ struct DecodeSmem {
     static constexpr size_t bars = ring;
     static constexpr size_t masks = bars + (size_t)W * S * 8;
     static constexpr size_t probs = masks + (size_t)W * S * 4;
-    static constexpr size_t total = probs + (size_t)W * kChunk * G * 4;
+    static constexpr size_t total = probs + (size_t)W * kChunk * G * 8;  // (p, p) pairs
     // the CTA combine reuses the ring: per warp 2G + G*D floats
     static_assert((size_t)W * (4 * G + G * 128) * 4 <= ring, "combine area must fit in the ring");
 };
@@ -195,7 +205,7 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
     unsigned char* ring = smem + (size_t)warp * S * 2 * kChunkBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars) + warp * S;
     uint32_t* masks = reinterpret_cast<uint32_t*>(smem + L::masks) + warp * S;
-    float* ps = reinterpret_cast<float*>(smem + L::probs) + warp * kChunk * G;
+    float2* ps = reinterpret_cast<float2*>(smem + L::probs) + warp * kChunk * G;
     __shared__ int aborted;
     if (threadIdx.x == 0) aborted = 0;
 
@@ -244,26 +254,29 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
     const int gx = G == 1 ? 0 : (lane & 1) * (G / 2);  // local head g holds head g^gx
     const int t_mine = 2 * jx + half;         // row of this lane's finished scores
 
-    // query registers, permuted by gx and pre-scaled into base-2 logits
-    float qreg[G][EPL];
+    // query registers (element pairs), permuted by gx, pre-scaled into base-2 logits
+    constexpr int EP = EPL / 2;
+    float2 q2[G][EP];
     {
         const T* qb = reinterpret_cast<const T*>(p.q) +
                       ((int64_t)s * p.num_q_heads + (int64_t)h * G) * D + col * EPL;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             const uint4 u = __ldg(reinterpret_cast<const uint4*>(qb + (int64_t)(g ^ gx) * D));
-            float f[EPL];
-            R::unpack(u, f);
+            float2 f[EP];
+            R::unpack2(u, f);
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) qreg[g][e] = f[e] * p.scale_log2;
+            for (int e = 0; e < EP; ++e)
+                q2[g][e] = make_float2(f[e].x * p.scale_log2, f[e].y * p.scale_log2);
         }
     }
 
-    float acc[G][EPL];
+    // P*V accumulators: element pairs of this lane's column, for every head
+    float2 acc[G][EP];
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[g][e] = 0.f;
+        for (int e = 0; e < EP; ++e) acc[g][e] = make_float2(0.f, 0.f);
     float m[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) m[g] = -INFINITY;
@@ -292,14 +305,15 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
         for (int j = 0; j < 8; ++j) {
             const int row = 2 * (j ^ jx) + half;
             const uint4 u = *reinterpret_cast<const uint4*>(kst + row * kRowBytes + col * 16);
-            float k[EPL];
-            R::unpack(u, k);
+            float2 k[EP];
+            R::unpack2(u, k);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                float a = 0.f;
+                // even and odd elements accumulate in the two halves of a packed FMA
+                float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) a = fmaf(qreg[g][e], k[e], a);
-                part[j * G + g] = a;
+                for (int e = 0; e < EP; ++e) a = __ffma2_rn(q2[g][e], k[e], a);
+                part[j * G + g] = a.x + a.y;
             }
         }
 #pragma unroll
@@ -347,8 +361,9 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
                 const float mn = fmaxf(m[g], cmax[g]);
                 corr[g] = ex2(m[g] - mn);
                 m[g] = mn;
+                const float2 c2 = make_float2(corr[g], corr[g]);
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[g][e] *= corr[g];
+                for (int e = 0; e < EP; ++e) acc[g][e] = __fmul2_rn(acc[g][e], c2);
             }
 #pragma unroll
             for (int x = 0; x < NSF; ++x) {
@@ -363,12 +378,13 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
             l_lane[x] += pr[x];
         }
 
-        // ---- broadcast probabilities of the 16 rows x G heads
+        // ---- broadcast probabilities of the 16 rows x G heads, each stored as a
+        //      (p, p) pair so the P*V packed FMAs read their operand directly
         if (G == 1) {
-            if ((lane & 1) == 0) ps[t_mine] = pr[0];
+            if ((lane & 1) == 0) ps[t_mine] = make_float2(pr[0], pr[0]);
         } else {
 #pragma unroll
-            for (int x = 0; x < NSF; ++x) ps[t_mine * G + gx + x] = pr[x];
+            for (int x = 0; x < NSF; ++x) ps[t_mine * G + gx + x] = make_float2(pr[x], pr[x]);
         }
         __syncwarp();
 
@@ -376,20 +392,20 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int row = 2 * j + half;
-            float pg[G];
+            float2 pg[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) pg[g] = ps[row * G + g];
             const uint4 u = *reinterpret_cast<const uint4*>(vst + row * kRowBytes + col * 16);
-            float v[EPL];
-            R::unpack(u, v);
+            float2 v[EP];
+            R::unpack2(u, v);
             if (masked && !((vmask >> row) & 1u)) {
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) v[e] = 0.f;  // unwritten rows may hold NaN
+                for (int e = 0; e < EP; ++e) v[e] = make_float2(0.f, 0.f);  // unwritten rows may hold NaN
             }
 #pragma unroll
             for (int g = 0; g < G; ++g)
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pg[g], v[e], acc[g][e]);
+                for (int e = 0; e < EP; ++e) acc[g][e] = __ffma2_rn(pg[g], v[e], acc[g][e]);
         }
         __syncwarp();
 
@@ -408,7 +424,10 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[g][e] += __shfl_xor_sync(kFull, acc[g][e], 16);
+        for (int e = 0; e < EP; ++e) {
+            acc[g][e].x += __shfl_xor_sync(kFull, acc[g][e].x, 16);
+            acc[g][e].y += __shfl_xor_sync(kFull, acc[g][e].y, 16);
+        }
 #pragma unroll
     for (int off = 2; off <= 16; off <<= 1)
 #pragma unroll
@@ -444,9 +463,9 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
-            for (int e = 0; e < EPL; e += 4)
-                *reinterpret_cast<float4*>(mine + g * D + col * EPL + e) =
-                    make_float4(acc[g][e], acc[g][e + 1], acc[g][e + 2], acc[g][e + 3]);
+            for (int e = 0; e < EP; e += 2)
+                *reinterpret_cast<float4*>(mine + g * D + col * EPL + 2 * e) =
+                    make_float4(acc[g][e].x, acc[g][e].y, acc[g][e + 1].x, acc[g][e + 1].y);
     }
     __syncthreads();
     const int64_t qh0 = (int64_t)s * p.num_q_heads + (int64_t)h * G;
@@ -502,8 +521,8 @@ __global__ void decode_merge_kernel(const DecodeParams p, int D) {
 
 // ---------------------------------------------------------------- host side
 constexpr int kWarps = 4;
-constexpr int kStages = 3;
-constexpr int kCtasPerSm = 2;
+constexpr int kStages = 2;
+constexpr int kCtasPerSm = 3;
 constexpr int kWaves = 6;
 
 struct Plan {

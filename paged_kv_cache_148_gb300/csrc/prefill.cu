@@ -21,7 +21,9 @@
 //   warps 2-5  softmax: thread r owns row r (TMEM lane r): loads S_j, masks,
 //           online softmax in base 2 with lazy rescaling of O (only when the
 //           row max grows by more than 2^8), writes P_j as bf16 into a
-//           128-byte-swizzled K-major tile, and finally normalises O.
+//           128-byte-swizzled K-major tile (plus its bf16 residual for
+//           tiles with short rows, see kPreciseBelow), and finally
+//           normalises O.
 // All mbarrier waits are bounded; a wait that runs out sets PA_ERR_TIMEOUT
 // and the CTA winds down.
 #include <cuda.h>
@@ -45,13 +47,19 @@ constexpr int kTile = 2 * kHalf;        // 32 KiB
 constexpr int kPfThreads = 192;
 constexpr uint32_t kTmemCols = 512;     // S0 | S1 | O (| unused)
 constexpr float kPfRescale = 8.0f;
+// A tile whose first row sees fewer keys than this runs P*V twice, on
+// bf16(P) and on the bf16 residual P - bf16(P): with few keys the 2^-9
+// rounding of a single bf16 P is visible in the output, with many keys it
+// averages out.
+constexpr int kPreciseBelow = 1024;
 
 // shared-memory map (offsets from a 1024-aligned base)
 constexpr int kOffQ = 0;
 constexpr int kOffK = kTile;            // 2 stages
 constexpr int kOffV = 3 * kTile;        // 2 stages
 constexpr int kOffP = 5 * kTile;
-constexpr int kOffBar = 6 * kTile;
+constexpr int kOffP2 = 6 * kTile;       // residual of P (precise tiles only)
+constexpr int kOffBar = 7 * kTile;
 constexpr int kPfSmem = kOffBar + 256 + 1024;  // + barriers, + alignment slack
 
 struct PrefillParams {
@@ -138,6 +146,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     const int pages_per_tile = kPfKeys >> p.log2_bp;
     // keys at or past `zlim` may be unwritten or not loaded: V rows there are zeroed
     const int zlim = min(ctx, ((kv_end + bp - 1) >> p.log2_bp) << p.log2_bp);
+    const bool precise = (p.causal ? base_pos + q0 + 1 : ctx) < kPreciseBelow;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -213,6 +222,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, 128, 0, 1);
             const uint32_t q_addr = smem_u32(smem + kOffQ);
             const uint32_t p_addr = smem_u32(smem + kOffP);
+            const uint32_t p2_addr = smem_u32(smem + kOffP2);
             bool ok = pf_wait(&bars->q_full, 0, bars, p.d_err);
             auto pv = [&](int t) -> bool {
                 if (!pf_wait(&bars->p_full, t & 1, bars, p.d_err)) return false;
@@ -220,9 +230,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 const uint32_t v_addr = smem_u32(smem + kOffV + (t & 1) * kTile);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t a = tc::smem_desc_sw128(p_addr + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
+                    const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
                     const uint64_t b = tc::smem_desc_sw128(v_addr + kk * 2048, kHalf, 1024);
-                    tc::mma_bf16(tO, a, b, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_bf16(tO, tc::smem_desc_sw128(p_addr + poff, 16, 1024), b, idesc_pv,
+                                 (t > 0 || kk > 0) ? 1u : 0u);
+                    if (precise)
+                        tc::mma_bf16(tO, tc::smem_desc_sw128(p2_addr + poff, 16, 1024), b, idesc_pv, 1u);
                 }
                 tc::commit(&bars->o_done);
                 tc::commit(&bars->kv_empty[t & 1]);
@@ -315,17 +328,34 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             // probabilities (masked keys give exactly 0)
             float lsum = 0.f;
             uint32_t pk[64];
+            if (!precise) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float a = ex2(__uint_as_float(sr[c][e]) - m_used);
-                    const float b2 = ex2(__uint_as_float(sr[c][e + 1]) - m_used);
-                    const uint32_t w = pack_bf16(a, b2);
-                    // the row sum uses the rounded weights the tensor cores see
-                    lsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
-                    pk[(c * 32 + e) >> 1] = w;
-                }
+                    for (int e = 0; e < 32; e += 2) {
+                        const float a = ex2(__uint_as_float(sr[c][e]) - m_used);
+                        const float b2 = ex2(__uint_as_float(sr[c][e + 1]) - m_used);
+                        const uint32_t w = pack_bf16(a, b2);
+                        // the row sum uses the rounded weights the tensor cores see
+                        lsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+                        pk[(c * 32 + e) >> 1] = w;
+                    }
+            } else {
+                // P = hi + lo, both bf16; hi goes to pk, lo overwrites sr's first half
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float a = ex2(__uint_as_float(sr[c][e]) - m_used);
+                        const float b2 = ex2(__uint_as_float(sr[c][e + 1]) - m_used);
+                        const uint32_t w = pack_bf16(a, b2);
+                        const float ra = a - __uint_as_float(w << 16);
+                        const float rb = b2 - __uint_as_float(w & 0xffff0000u);
+                        lsum += a + b2;
+                        pk[(c * 32 + e) >> 1] = w;
+                        sr[c][e >> 1] = pack_bf16(ra, rb);
+                    }
+            }
             l += lsum;
             // the P tile is single-buffered: PV_{j-1} must have finished reading it
             if (j >= 1 && !o_ready) {
@@ -350,6 +380,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             for (int c = 0; c < 16; ++c) {
                 const uint32_t addr = p_row + (c >> 3) * kHalf + (((c & 7) ^ (r & 7)) << 4);
                 st_shared_v4(addr, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            }
+            if (precise) {
+                // residual pairs for keys 2k, 2k+1 sit in sr[k / 16][k % 16]
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint32_t addr = p_row + (kOffP2 - kOffP) + (c >> 3) * kHalf +
+                                          (((c & 7) ^ (r & 7)) << 4);
+                    const int k0 = 4 * c;  // first packed pair of this chunk
+                    st_shared_v4(addr, sr[k0 >> 4][k0 & 15], sr[(k0 + 1) >> 4][(k0 + 1) & 15],
+                                 sr[(k0 + 2) >> 4][(k0 + 2) & 15], sr[(k0 + 3) >> 4][(k0 + 3) & 15]);
+                }
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars->p_full);
