@@ -211,6 +211,27 @@ pa_status pa_decode_merge(const pa_kv_pool* pool, int32_t num_q_heads,
                           size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_decode without a caller-provided workspace, for callers that cannot
+ * allocate device memory when they run decode: code being recorded into a
+ * CUDA graph (no cudaMalloc while a capture is open), plugin hosts that pass
+ * raw pointers but no allocator, and processes whose HBM is all given to the
+ * block pool.  The pages have no counterpart to this entry point.
+ * Same arguments and results as pa_decode minus workspace/workspace_bytes.
+ * The split-KV partials live in a static device array of 16 MiB that the
+ * library's device image carries (every GPU that loads the library holds it
+ * until the process exits).  A shape whose pa_decode_workspace_bytes exceeds
+ * 16 MiB returns PA_ERR_UNSUPPORTED and enqueues nothing.  Allocates nothing.
+ * The first call on each device (with that device current) looks up the
+ * array's address; make it before any stream capture.  All calls share the
+ * array: calls that may overlap on the GPU (unordered streams) race.
+ */
+pa_status pa_decode_noalloc(const pa_kv_pool* pool, const void* q, int32_t num_q_heads,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* context_lens, int32_t num_seqs, int32_t max_context,
+                            float scale, int32_t partition_tokens, float* out, int32_t* d_err,
+                            pa_stream_t stream);
+
+/*
  * Paged chunked-prefill attention on tensor cores (P1 §4: prefill reuses a
  * flash-style tiled kernel fed the paged table; paging and IO-aware tiling
  * are orthogonal).  Sequence s has new query tokens

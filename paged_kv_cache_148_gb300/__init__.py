@@ -40,7 +40,7 @@ EXPORTED = [
     "pa_status_str", "pa_last_cuda_error", "pa_abi_version", "pa_page_size_bytes",
     "pa_physical_slot", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks",
     "pa_decode_partition_tokens", "pa_decode_workspace_bytes", "pa_decode", "pa_decode_partial",
-    "pa_decode_merge", "pa_prefill",
+    "pa_decode_merge", "pa_decode_noalloc", "pa_prefill",
     "pa_alloc_create", "pa_alloc_destroy", "pa_alloc_append", "pa_alloc_fork",
     "pa_alloc_writable_tail", "pa_alloc_reserve", "pa_alloc_release", "pa_alloc_refcount",
     "pa_alloc_num_free",
@@ -94,6 +94,7 @@ def lib() -> ctypes.CDLL:
         "pa_decode": ([P, P, i32, P, i32, P, i32, i32, f32, i32, P, P, sz, P, P], i32),
         "pa_decode_partial": ([P, P, i32, P, i32, P, i32, i32, f32, i32, P, P, sz, P, P], i32),
         "pa_decode_merge": ([P, i32, P, i32, i32, i32, P, P, sz, P], i32),
+        "pa_decode_noalloc": ([P, P, i32, P, i32, P, i32, i32, f32, i32, P, P, P], i32),
         "pa_prefill": ([P, P, i32, i32, P, P, P, i32, i32, i32, i32, f32, i32, P, P, P], i32),
         "pa_alloc_create": ([i32, P, P], i32),
         "pa_alloc_destroy": ([P], None),

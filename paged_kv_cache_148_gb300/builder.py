@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpagedkv.so")
-SOURCES = ["host.cpp", "write_copy.cu", "decode.cu", "prefill.cu"]
+SOURCES = ["host.cpp", "write_copy.cu", "decode.cu", "decode_noalloc.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 
