@@ -20,10 +20,15 @@
 //           P_{j-1}; tcgen05.commit signals completion on mbarriers.
 //   warps 2-5  softmax: thread r owns row r (TMEM lane r): loads S_j, masks,
 //           online softmax in base 2 with lazy rescaling of O (only when the
-//           row max grows by more than 2^8), writes P_j as bf16 into a
-//           128-byte-swizzled K-major tile (plus its bf16 residual for
-//           tiles with short rows, see kPreciseBelow), and finally
-//           normalises O.
+//           row max grows by more than 2^8), converts its key row of the V
+//           tile from bf16 to fp16 in place, writes P_j as fp16 into a
+//           128-byte-swizzled K-major tile, and finally normalises O.
+// Q K^T runs on bf16 operands; P V runs on fp16 operands: P in [0, 2^8]
+// keeps 11 significant bits in fp16 against 8 in bf16, which the stated
+// accuracy needs (bf16 P alone leaves ~1.6e-3 relative L2 error at 2.5K
+// keys).  bf16 -> fp16 is exact for |v| <= 65504 (the fp16 range; larger
+// magnitudes saturate to +-65504) apart from fp16 subnormals below 2^-14,
+// whose absolute error stays under 2^-25.
 // All mbarrier waits are bounded; a wait that runs out sets PA_ERR_TIMEOUT
 // and the CTA winds down.
 #include <cuda.h>
@@ -47,19 +52,13 @@ constexpr int kTile = 2 * kHalf;        // 32 KiB
 constexpr int kPfThreads = 192;
 constexpr uint32_t kTmemCols = 512;     // S0 | S1 | O (| unused)
 constexpr float kPfRescale = 8.0f;
-// A tile whose first row sees fewer keys than this runs P*V twice, on
-// bf16(P) and on the bf16 residual P - bf16(P): with few keys the 2^-9
-// rounding of a single bf16 P is visible in the output, with many keys it
-// averages out.
-constexpr int kPreciseBelow = 1024;
 
 // shared-memory map (offsets from a 1024-aligned base)
 constexpr int kOffQ = 0;
 constexpr int kOffK = kTile;            // 2 stages
 constexpr int kOffV = 3 * kTile;        // 2 stages
 constexpr int kOffP = 5 * kTile;
-constexpr int kOffP2 = 6 * kTile;       // residual of P (precise tiles only)
-constexpr int kOffBar = 7 * kTile;
+constexpr int kOffBar = 6 * kTile;
 constexpr int kPfSmem = kOffBar + 256 + 1024;  // + barriers, + alignment slack
 
 struct PrefillParams {
@@ -90,9 +89,34 @@ struct PfBars {
     int32_t abort;
 };
 
-PA_DEVICE uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
+// two floats -> fp16 pair (lo in the low half)
+PA_DEVICE uint32_t pack_f16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// bf16 pair -> fp16 pair (saturating at the fp16 range)
+PA_DEVICE uint32_t bf16x2_to_f16x2(uint32_t w) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+        : "=r"(r) : "f"(__uint_as_float(w & 0xffff0000u)), "f"(__uint_as_float(w << 16)));
+    return r;
+}
+
+// acc + lo + hi of an fp16 pair, accumulated in fp32
+PA_DEVICE float add_f16x2_to(float acc, uint32_t h2) {
+    float r;
+    asm("{ .reg .b16 a, b; mov.b32 {a, b}, %1; add.rn.f32.f16 %0, a, %2; add.rn.f32.f16 %0, b, %0; }"
+        : "=f"(r) : "r"(h2), "f"(acc));
+    return r;
+}
+
+PA_DEVICE uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
 }
 
 PA_DEVICE void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -146,7 +170,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     const int pages_per_tile = kPfKeys >> p.log2_bp;
     // keys at or past `zlim` may be unwritten or not loaded: V rows there are zeroed
     const int zlim = min(ctx, ((kv_end + bp - 1) >> p.log2_bp) << p.log2_bp);
-    const bool precise = (p.causal ? base_pos + q0 + 1 : ctx) < kPreciseBelow;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -219,10 +242,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, 128, 0, 0);
-            constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, 128, 0, 1);
+            constexpr uint32_t idesc_pv = tc::idesc_f16_f32(128, 128, 0, 1);
             const uint32_t q_addr = smem_u32(smem + kOffQ);
             const uint32_t p_addr = smem_u32(smem + kOffP);
-            const uint32_t p2_addr = smem_u32(smem + kOffP2);
             bool ok = pf_wait(&bars->q_full, 0, bars, p.d_err);
             auto pv = [&](int t) -> bool {
                 if (!pf_wait(&bars->p_full, t & 1, bars, p.d_err)) return false;
@@ -234,8 +256,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     const uint64_t b = tc::smem_desc_sw128(v_addr + kk * 2048, kHalf, 1024);
                     tc::mma_bf16(tO, tc::smem_desc_sw128(p_addr + poff, 16, 1024), b, idesc_pv,
                                  (t > 0 || kk > 0) ? 1u : 0u);
-                    if (precise)
-                        tc::mma_bf16(tO, tc::smem_desc_sw128(p2_addr + poff, 16, 1024), b, idesc_pv, 1u);
                 }
                 tc::commit(&bars->o_done);
                 tc::commit(&bars->kv_empty[t & 1]);
@@ -326,53 +346,46 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 }
             }
             // probabilities (masked keys give exactly 0)
+            // probabilities in fp16; the row sum adds the rounded values the
+            // tensor cores multiply with
             float lsum = 0.f;
             uint32_t pk[64];
-            if (!precise) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const float a = ex2(__uint_as_float(sr[c][e]) - m_used);
-                        const float b2 = ex2(__uint_as_float(sr[c][e + 1]) - m_used);
-                        const uint32_t w = pack_bf16(a, b2);
-                        // the row sum uses the rounded weights the tensor cores see
-                        lsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
-                        pk[(c * 32 + e) >> 1] = w;
-                    }
-            } else {
-                // P = hi + lo, both bf16; hi goes to pk, lo overwrites sr's first half
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const float a = ex2(__uint_as_float(sr[c][e]) - m_used);
-                        const float b2 = ex2(__uint_as_float(sr[c][e + 1]) - m_used);
-                        const uint32_t w = pack_bf16(a, b2);
-                        const float ra = a - __uint_as_float(w << 16);
-                        const float rb = b2 - __uint_as_float(w & 0xffff0000u);
-                        lsum += a + b2;
-                        pk[(c * 32 + e) >> 1] = w;
-                        sr[c][e >> 1] = pack_bf16(ra, rb);
-                    }
-            }
+                for (int e = 0; e < 32; e += 2) {
+                    const float a = ex2(__uint_as_float(sr[c][e]) - m_used);
+                    const float b2 = ex2(__uint_as_float(sr[c][e + 1]) - m_used);
+                    const uint32_t w = pack_f16(a, b2);
+                    lsum = add_f16x2_to(lsum, w);
+                    pk[(c * 32 + e) >> 1] = w;
+                }
             l += lsum;
             // the P tile is single-buffered: PV_{j-1} must have finished reading it
             if (j >= 1 && !o_ready) {
                 ok = pf_wait(&bars->o_done, (j - 1) & 1, bars, p.d_err);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             }
-            if (key0 + kPfKeys > zlim) {
-                // last tile: V rows past the written/loaded keys may hold NaN; zero them
-                ok = pf_wait(&bars->kv_full[sb], (j >> 1) & 1, bars, p.d_err);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                if (key0 + r >= zlim) {
-                    const uint32_t vrow = smem_u32(smem + kOffV + sb * kTile) + r * 128;
+            // this thread's key row of V_j: bf16 -> fp16 in place (16-byte chunks keep
+            // their swizzled positions); rows past the written keys become zeros
+            ok = pf_wait(&bars->kv_full[sb], (j >> 1) & 1, bars, p.d_err);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            {
+                const uint32_t vrow = smem_u32(smem + kOffV + sb * kTile) + r * 128;
+                // chunk order rotated by the row so the 8 threads of a 128-bit access
+                // phase touch 8 different bank groups
+                if (key0 + r < zlim) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        st_shared_v4(vrow + c * 16, 0, 0, 0, 0);
-                        st_shared_v4(vrow + kHalf + c * 16, 0, 0, 0, 0);
+                    for (int c = 0; c < 16; ++c) {
+                        const uint32_t a = vrow + (c >> 3) * kHalf + ((c + r) & 7) * 16;
+                        const uint4 x = ld_shared_v4(a);
+                        st_shared_v4(a, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y),
+                                     bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
                     }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        st_shared_v4(vrow + (c >> 3) * kHalf + ((c + r) & 7) * 16, 0, 0, 0, 0);
                 }
             }
             // P row r: 16-byte chunk c (keys 8c..8c+7) at chunk (c mod 8) ^ (r mod 8) of half c/8
@@ -380,17 +393,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             for (int c = 0; c < 16; ++c) {
                 const uint32_t addr = p_row + (c >> 3) * kHalf + (((c & 7) ^ (r & 7)) << 4);
                 st_shared_v4(addr, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            }
-            if (precise) {
-                // residual pairs for keys 2k, 2k+1 sit in sr[k / 16][k % 16]
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const uint32_t addr = p_row + (kOffP2 - kOffP) + (c >> 3) * kHalf +
-                                          (((c & 7) ^ (r & 7)) << 4);
-                    const int k0 = 4 * c;  // first packed pair of this chunk
-                    st_shared_v4(addr, sr[k0 >> 4][k0 & 15], sr[(k0 + 1) >> 4][(k0 + 1) & 15],
-                                 sr[(k0 + 2) >> 4][(k0 + 2) & 15], sr[(k0 + 3) >> 4][(k0 + 3) & 15]);
-                }
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars->p_full);

@@ -57,8 +57,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          | ((uint32_t)(M >> 4) << 24);    // M / 16
 }
 
+// The same for fp16 A/B (formats 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4)                      // D format: f32
+         | ((uint32_t)a_mn << 15)
+         | ((uint32_t)b_mn << 16)
+         | ((uint32_t)(N >> 3) << 17)
+         | ((uint32_t)(M >> 4) << 24);
+}
+
 // ----------------------------------------------------------------- MMA
-// D[tmem] (+)= A[smem desc] * B[smem desc]; issued by one thread.
+// D[tmem] (+)= A[smem desc] * B[smem desc] (kind::f16: bf16 or fp16 operands,
+// per the instruction descriptor); issued by one thread.
 PA_DEVICE void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                         uint32_t accumulate) {
     asm volatile(
