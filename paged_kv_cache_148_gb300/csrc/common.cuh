@@ -39,6 +39,15 @@ PA_DEVICE uint64_t global_timer_ns() {
     return t;
 }
 
+// ----------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while its predecessor in the stream is finishing;
+// griddep_wait() blocks until the predecessor grid has completed and its
+// memory is visible (a no-op for an ordinary launch).  griddep_launch()
+// lets the next kernel in the stream start launching.
+PA_DEVICE void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+PA_DEVICE void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------------------------------------------- mbarrier
 PA_DEVICE void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));

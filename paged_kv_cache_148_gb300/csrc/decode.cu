@@ -189,19 +189,32 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
     static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group size");
 
     const int s = blockIdx.x, h = blockIdx.y, part = blockIdx.z;
+    griddep_wait();  // K/V rows, tables and lengths may come from the previous kernel
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c_begin = part * p.part_chunks;
+    const int first = c_begin + warp;  // this warp's chunks: first + i*W
+    const bool big_pages = p.log2_bp >= 4;
+    const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks;
+    // block-table prefetch, issued together with the length load below: lane j
+    // holds the id of local chunk (base + j); entries past the sequence are
+    // in the table row and never used
+    auto table_id = [&](int i) -> int32_t {
+        const int c = first + i * W;
+        const int e = (c * kChunk) >> p.log2_bp;
+        return e < p.max_blocks ? __ldg(table + e) : -1;
+    };
+    int32_t id_reg = big_pages ? table_id(lane) : -1;
     int n = __ldg(p.context_lens + s);
     if (n > p.max_parts * p.part_chunks * kChunk) {  // longer than the plan's max_context
         if (part == 0 && h == 0 && threadIdx.x == 0) set_error(p.d_err, PA_ERR_OUT_OF_RANGE);
         n = p.max_parts * p.part_chunks * kChunk;
     }
     const int n_chunks = (n + kChunk - 1) / kChunk;
-    const int c_begin = part * p.part_chunks;
     if (n <= 0 || c_begin >= n_chunks) return;
     const int c_end = min(c_begin + p.part_chunks, n_chunks);
     const int n_parts = (n_chunks + p.part_chunks - 1) / p.part_chunks;
 
     extern __shared__ __align__(128) unsigned char smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned char* ring = smem + (size_t)warp * S * 2 * kChunkBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars) + warp * S;
     uint32_t* masks = reinterpret_cast<uint32_t*>(smem + L::masks) + warp * S;
@@ -216,19 +229,7 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
     }
     __syncthreads();
 
-    // this warp's chunks: c_begin + warp + i*W
-    const int first = c_begin + warp;
     const int my_n = first < c_end ? (c_end - first + W - 1) / W : 0;
-    const bool big_pages = p.log2_bp >= 4;
-    const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks;
-
-    // block-table prefetch: lane j holds the id of local chunk (base + j)
-    auto table_id = [&](int i) -> int32_t {
-        const int c = first + i * W;
-        const int e = (c * kChunk) >> p.log2_bp;
-        return e < p.max_blocks ? __ldg(table + e) : -1;
-    };
-    int32_t id_reg = (big_pages && lane < my_n) ? table_id(lane) : -1;
     int id_base = 0;
 
     // the error check for the table width happens at issue time
@@ -419,6 +420,7 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
         if (lane == 0 && nxt < my_n) issue(nxt, nid);
     }
     if (!ok) aborted = 1;
+    griddep_launch();  // the merge may start launching; it waits for this grid to finish
 
     // ---- finish this warp's state
 #pragma unroll
@@ -495,35 +497,69 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
 }
 
 // Merge of split-KV partials (P1 §4): M = max m_p, L = sum l_p 2^(m_p - M),
-// out = sum acc_p 2^(m_p - M) / L.  One CTA per (sequence, q-head), one
-// thread per output element.
-__global__ void decode_merge_kernel(const DecodeParams p, int D) {
+// out = sum acc_p 2^(m_p - M) / L.  One CTA per (sequence, q-head): the
+// partition maxima and sums are loaded in parallel (one per thread) into
+// shared memory, then every thread sums its output element over the
+// partitions with independent loads.
+constexpr int kMergeThreads = 128;
+constexpr int kMergeMaxParts = 1024;  // partitions handled per pass through shared memory
+
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p, int D) {
     const int s = blockIdx.x / p.num_q_heads;
     const int g = blockIdx.x - s * p.num_q_heads;
+    griddep_wait();  // partials come from the partition kernel
     const int n = __ldg(p.context_lens + s);
     if (n <= 0) return;
     const int n_chunks = (n + kChunk - 1) / kChunk;
     const int n_parts = min((n_chunks + p.part_chunks - 1) / p.part_chunks, p.max_parts);
     if (n_parts <= 1) return;
+    __shared__ float wts[kMergeMaxParts];
+    __shared__ float red[kMergeThreads / 32];
     const int64_t base = ((int64_t)s * p.num_q_heads + g) * p.max_parts;
+    const int tid = threadIdx.x;
+    // global max over partitions
     float M = -INFINITY;
-    for (int i = 0; i < n_parts; ++i) M = fmaxf(M, p.ws_m[base + i]);
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float Lsum = 0.f, A = 0.f;
-        for (int i = 0; i < n_parts; ++i) {
-            const float c = ex2(p.ws_m[base + i] - M);
-            Lsum = fmaf(p.ws_l[base + i], c, Lsum);
-            A = fmaf(p.ws_acc[(base + i) * D + d], c, A);
+    for (int i = tid; i < n_parts; i += kMergeThreads) M = fmaxf(M, p.ws_m[base + i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+    if ((tid & 31) == 0) red[tid >> 5] = M;
+    __syncthreads();
+    M = red[0];
+#pragma unroll
+    for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red[w]);
+    float acc[2] = {0.f, 0.f}, L = 0.f;
+    for (int p0 = 0; p0 < n_parts; p0 += kMergeMaxParts) {
+        const int cnt = min(kMergeMaxParts, n_parts - p0);
+        __syncthreads();
+        for (int i = tid; i < cnt; i += kMergeThreads) wts[i] = ex2(p.ws_m[base + p0 + i] - M);
+        for (int i = tid; i < cnt; i += kMergeThreads) L = fmaf(p.ws_l[base + p0 + i], wts[i], L);
+        __syncthreads();
+        const float* a = p.ws_acc + (base + p0) * D;
+#pragma unroll 4
+        for (int i = 0; i < cnt; ++i) {
+            const float w = wts[i];
+            if (tid < D) acc[0] = fmaf(a[(int64_t)i * D + tid], w, acc[0]);
+            if (tid + kMergeThreads < D) acc[1] = fmaf(a[(int64_t)i * D + tid + kMergeThreads], w, acc[1]);
         }
-        p.out[((int64_t)s * p.num_q_heads + g) * D + d] = A / Lsum;
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+    __syncthreads();
+    if ((tid & 31) == 0) red[tid >> 5] = L;
+    __syncthreads();
+    L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeThreads / 32; ++w) L += red[w];
+    float* o = p.out + ((int64_t)s * p.num_q_heads + g) * D;
+    if (tid < D) o[tid] = acc[0] / L;
+    if (tid + kMergeThreads < D) o[tid + kMergeThreads] = acc[1] / L;
 }
 
 // ---------------------------------------------------------------- host side
 constexpr int kWarps = 4;
 constexpr int kStages = 2;
 constexpr int kCtasPerSm = 3;
-constexpr int kWaves = 6;
+constexpr int kWaves = 9;
 
 struct Plan {
     int32_t part_chunks;
@@ -584,7 +620,11 @@ static pa_status launch_partial(const DecodeParams& prm, int32_t B, int32_t Hkv,
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
     dim3 grid((unsigned)B, (unsigned)Hkv, (unsigned)max_parts);
-    kern<<<grid, kWarps * 32, Lay::total, stream>>>(prm);
+    cudaError_t e = launch_pdl(kern, grid, dim3(kWarps * 32), Lay::total, stream, prm);
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PA_ERR_CUDA;
+    }
     return launch_status();
 }
 
@@ -713,8 +753,12 @@ extern "C" pa_status pa_decode_merge(const pa_kv_pool* pool, int32_t num_q_heads
     prm.out = out;
     bind_workspace(plan, workspace, &prm);
     const int D = pool->head_dim;
-    decode_merge_kernel<<<(unsigned)((int64_t)num_seqs * num_q_heads), D <= 128 ? 128 : 256, 0,
-                          (cudaStream_t)stream>>>(prm, D);
+    cudaError_t e = launch_pdl(decode_merge_kernel, dim3((unsigned)((int64_t)num_seqs * num_q_heads)),
+                               dim3(kMergeThreads), 0, (cudaStream_t)stream, prm, D);
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PA_ERR_CUDA;
+    }
     return launch_status();
 }
 

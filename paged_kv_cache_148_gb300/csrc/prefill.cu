@@ -14,7 +14,10 @@
 // pool through the block table.
 //
 // Roles (192 threads):
-//   warp 0  TMA producer: Q tile once, then K/V tiles into a 2-stage ring.
+//   warp 0  TMA producer: Q tile once, then K tiles into a 3-stage ring
+//           (a stage frees when its S MMA completes) and V tiles into a
+//           2-stage ring (freed when its P*V MMA completes), issuing
+//           whichever load has a free stage.
 //   warp 1  MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
 //           buffers, then O += P_{j-1} V_{j-1} once the softmax published
 //           P_{j-1}; tcgen05.commit signals completion on mbarriers.
@@ -54,12 +57,14 @@ constexpr uint32_t kTmemCols = 512;     // S0 | S1 | O (| unused)
 constexpr float kPfRescale = 8.0f;
 
 // shared-memory map (offsets from a 1024-aligned base)
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
 constexpr int kOffQ = 0;
-constexpr int kOffK = kTile;            // 2 stages
-constexpr int kOffV = 3 * kTile;        // 2 stages
-constexpr int kOffP = 5 * kTile;
-constexpr int kOffBar = 6 * kTile;
-constexpr int kPfSmem = kOffBar + 256 + 1024;  // + barriers, + alignment slack
+constexpr int kOffK = kTile;                         // kKStages stages
+constexpr int kOffV = kOffK + kKStages * kTile;      // kVStages stages
+constexpr int kOffP = kOffV + kVStages * kTile;
+constexpr int kOffBar = kOffP + kTile;
+constexpr int kPfSmem = kOffBar + 1024 + 1024;  // + barriers and page ids, + alignment slack
 
 struct PrefillParams {
     const int32_t* cu_seqlens_q;
@@ -77,10 +82,15 @@ struct PrefillParams {
     int32_t* d_err;
 };
 
+constexpr int kIdRing = 4;  // tiles of page ids kept for the V loads (K runs <= 3 tiles ahead)
+
 struct PfBars {
+    int32_t page_row[kIdRing][32];  // pool row of each page of a tile (128 / B_p <= 16 used)
     uint64_t q_full;
-    uint64_t kv_full[2];
-    uint64_t kv_empty[2];
+    uint64_t k_full[kKStages];
+    uint64_t k_empty[kKStages];
+    uint64_t v_full[kVStages];
+    uint64_t v_empty[kVStages];
     uint64_t s_full[2];
     uint64_t s_empty[2];
     uint64_t p_full;
@@ -179,9 +189,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(&bars->k_full[i], 1);
+            mbar_init(&bars->k_empty[i], 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(&bars->v_full[i], 1);
+            mbar_init(&bars->v_empty[i], 1);
+        }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars->kv_full[i], 1);
-            mbar_init(&bars->kv_empty[i], 1);
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->s_empty[i], 128);
         }
@@ -203,6 +219,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        // The whole warp works: lane k handles page k of a tile (one coalesced
+        // table load per tile, prefetched a tile ahead, then its own TMA loads);
+        // lane 0 arms the barriers and decides when a stage is free.
+        const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks;
+        auto load_rows = [&](int j) -> int32_t {  // this lane's page of tile j
+            const int e = j * pages_per_tile + lane;
+            if (lane >= pages_per_tile || (e << p.log2_bp) >= kv_end) return -1;
+            int32_t id = e < p.max_blocks ? __ldg(table + e) : -1;
+            if (id < 0 || id >= p.num_blocks) {
+                set_error(p.d_err, id < 0 ? PA_ERR_NEGATIVE_BLOCK : PA_ERR_OUT_OF_RANGE);
+                id = 0;  // stay in bounds; the result is flagged as invalid
+            }
+            return (id * p.num_kv_heads + h) << p.log2_bp;
+        };
+        auto loaded_pages = [&](int j) {
+            const int rem = kv_end - j * kPfKeys;
+            return min(pages_per_tile, (rem + bp - 1) >> p.log2_bp);
+        };
         if (lane == 0) {
             tc::prefetch_tmap(&tmap_q);
             tc::prefetch_tmap(&tmap_k);
@@ -210,32 +244,72 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             mbar_arrive_expect_tx(&bars->q_full, kTile);
             tc::tma_load_3d(smem + kOffQ, &tmap_q, 0, h * G, q_begin + q0, &bars->q_full);
             tc::tma_load_3d(smem + kOffQ + kHalf, &tmap_q, 64, h * G, q_begin + q0, &bars->q_full);
-            const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !pf_wait(&bars->kv_empty[st], ((j >> 1) - 1) & 1, bars, p.d_err)) break;
-                const int e0 = j * pages_per_tile;
-                int loaded = 0;
-                for (int k = 0; k < pages_per_tile; ++k)
-                    if (((e0 + k) << p.log2_bp) < kv_end) ++loaded;
-                mbar_arrive_expect_tx(&bars->kv_full[st], (uint32_t)loaded * bp * 128 * 2 * 2);
-                unsigned char* kst = smem + kOffK + st * kTile;
-                unsigned char* vst = smem + kOffV + st * kTile;
-                for (int k = 0; k < loaded; ++k) {
-                    const int e = e0 + k;
-                    int32_t id = e < p.max_blocks ? __ldg(table + e) : -1;
-                    if (id < 0 || id >= p.num_blocks) {
-                        set_error(p.d_err, id < 0 ? PA_ERR_NEGATIVE_BLOCK : PA_ERR_OUT_OF_RANGE);
-                        id = 0;  // stay in bounds; the result is flagged as invalid
-                    }
-                    const int row = (id * p.num_kv_heads + h) << p.log2_bp;
-                    const int off = k * bp * 128;
-                    tc::tma_load_2d(kst + off, &tmap_k, 0, row, &bars->kv_full[st]);
-                    tc::tma_load_2d(kst + kHalf + off, &tmap_k, 64, row, &bars->kv_full[st]);
-                    tc::tma_load_2d(vst + off, &tmap_v, 0, row, &bars->kv_full[st]);
-                    tc::tma_load_2d(vst + kHalf + off, &tmap_v, 64, row, &bars->kv_full[st]);
+        }
+        int32_t next_row = load_rows(0);  // prefetched ids of tile kn
+        int kn = 0, vn = 0;
+        uint64_t t_idle = 0;
+        uint32_t spins = 0;
+        while (kn < n_tiles || vn < n_tiles) {
+            bool moved = false;
+            // K tile kn into its stage once the S MMA of tile kn - 3 has completed
+            int go = 0;
+            if (lane == 0)
+                go = kn < n_tiles && kn < vn + kIdRing &&  // page ids of tiles vn..kn stay live
+                     (kn < kKStages || mbar_try_wait(&bars->k_empty[kn % kKStages],
+                                                     ((kn / kKStages) - 1) & 1));
+            if (__shfl_sync(0xffffffffu, go, 0)) {
+                const int row = next_row;
+                if (kn + 1 < n_tiles) next_row = load_rows(kn + 1);
+                bars->page_row[kn % kIdRing][lane] = row;
+                const int loaded = loaded_pages(kn);
+                uint64_t* bar = &bars->k_full[kn % kKStages];
+                if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)loaded * bp * 128 * 2);
+                __syncwarp();
+                if (lane < loaded) {
+                    unsigned char* dst = smem + kOffK + (kn % kKStages) * kTile + lane * bp * 128;
+                    tc::tma_load_2d(dst, &tmap_k, 0, row, bar);
+                    tc::tma_load_2d(dst + kHalf, &tmap_k, 64, row, bar);
+                }
+                ++kn;
+                moved = true;
+            }
+            // V tile vn once the P*V MMA of tile vn - 2 has completed
+            go = 0;
+            if (lane == 0)
+                go = vn < n_tiles && vn < kn &&
+                     (vn < kVStages || mbar_try_wait(&bars->v_empty[vn % kVStages],
+                                                     ((vn / kVStages) - 1) & 1));
+            if (__shfl_sync(0xffffffffu, go, 0)) {
+                const int row = bars->page_row[vn % kIdRing][lane];
+                const int loaded = loaded_pages(vn);
+                uint64_t* bar = &bars->v_full[vn % kVStages];
+                if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)loaded * bp * 128 * 2);
+                __syncwarp();
+                if (lane < loaded) {
+                    unsigned char* dst = smem + kOffV + (vn % kVStages) * kTile + lane * bp * 128;
+                    tc::tma_load_2d(dst, &tmap_v, 0, row, bar);
+                    tc::tma_load_2d(dst + kHalf, &tmap_v, 64, row, bar);
+                }
+                ++vn;
+                moved = true;
+            }
+            if (moved) {
+                t_idle = 0;
+                continue;
+            }
+            int stop = 0;
+            if (lane == 0 && (++spins & 255u) == 0) {
+                if (*(volatile int32_t*)&bars->abort) stop = 1;
+                const uint64_t now = global_timer_ns();
+                if (t_idle == 0) {
+                    t_idle = now;
+                } else if (now - t_idle > kWaitLimitNs) {
+                    set_error(p.d_err, PA_ERR_TIMEOUT);
+                    *(volatile int32_t*)&bars->abort = 1;
+                    stop = 1;
                 }
             }
+            if (__shfl_sync(0xffffffffu, stop, 0)) break;
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -249,7 +323,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             auto pv = [&](int t) -> bool {
                 if (!pf_wait(&bars->p_full, t & 1, bars, p.d_err)) return false;
                 tc::fence_after_sync();
-                const uint32_t v_addr = smem_u32(smem + kOffV + (t & 1) * kTile);
+                const uint32_t v_addr = smem_u32(smem + kOffV + (t % kVStages) * kTile);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -258,15 +332,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                                  (t > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc::commit(&bars->o_done);
-                tc::commit(&bars->kv_empty[t & 1]);
+                tc::commit(&bars->v_empty[t % kVStages]);
                 return true;
             };
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int st = j & 1;
-                if (!pf_wait(&bars->kv_full[st], (j >> 1) & 1, bars, p.d_err)) { ok = false; break; }
+                const int ks = j % kKStages;
+                if (!pf_wait(&bars->k_full[ks], (j / kKStages) & 1, bars, p.d_err)) { ok = false; break; }
                 if (j >= 2 && !pf_wait(&bars->s_empty[st], ((j >> 1) - 1) & 1, bars, p.d_err)) { ok = false; break; }
                 tc::fence_after_sync();
-                const uint32_t k_addr = smem_u32(smem + kOffK + st * kTile);
+                const uint32_t k_addr = smem_u32(smem + kOffK + ks * kTile);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -275,6 +350,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     tc::mma_bf16(tS + st * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 tc::commit(&bars->s_full[st]);
+                tc::commit(&bars->k_empty[ks]);
                 if (j >= 1 && !pv(j - 1)) { ok = false; break; }
             }
             if (ok) pv(n_tiles - 1);
@@ -368,10 +444,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             }
             // this thread's key row of V_j: bf16 -> fp16 in place (16-byte chunks keep
             // their swizzled positions); rows past the written keys become zeros
-            ok = pf_wait(&bars->kv_full[sb], (j >> 1) & 1, bars, p.d_err);
+            ok = pf_wait(&bars->v_full[j % kVStages], (j / kVStages) & 1, bars, p.d_err);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             {
-                const uint32_t vrow = smem_u32(smem + kOffV + sb * kTile) + r * 128;
+                const uint32_t vrow = smem_u32(smem + kOffV + (j % kVStages) * kTile) + r * 128;
                 // chunk order rotated by the row so the 8 threads of a 128-bit access
                 // phase touch 8 different bank groups
                 if (key0 + r < zlim) {

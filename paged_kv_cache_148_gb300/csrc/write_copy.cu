@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256) write_kv_kernel(
     const uint4* __restrict__ v_new, const int64_t* __restrict__ slot_mapping, int64_t total_vecs,
     int32_t row_vecs, int32_t num_kv_heads, int32_t block_size, int64_t num_slots,
     int32_t* d_err) {
+    griddep_wait();
+    griddep_launch();  // the attention kernel that follows may start launching
     const int64_t per_token = (int64_t)row_vecs * num_kv_heads;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total_vecs;
          i += (int64_t)gridDim.x * blockDim.x) {
