@@ -1,5 +1,5 @@
 // pa_prefill: paged chunked-prefill attention on the 5th-generation tensor
-// cores (tcgen05, accumulators in TMEM, operands staged by TMA).
+// cores (tcgen05, accumulators and P in TMEM, operands staged by TMA).
 //
 // Semantics: "03｜PagedAttention 与 KV Cache 内存系统" §4 — prefill reuses a
 // flash-style tiled attention kernel that is handed the paged block table
@@ -7,25 +7,29 @@
 // through them).  New token i of a sequence sits at position
 // context_len - n_new + i and, with a causal mask, sees positions 0..itself.
 //
-// CTA = (q-tile, kv-head, sequence).  A tile is 128 rows = (128/G) queries x
-// the G query heads that share one kv-head, so every K/V byte staged in
-// shared memory feeds all G heads.  Key tiles are 128 keys = 128/B_p pages,
-// each page half (64 dims) fetched by one tiled TMA load straight from the
-// pool through the block table.
+// CTA = (pair of q-tiles, kv-head, sequence).  A q-tile is 128 rows =
+// (128/G) queries x the G query heads that share one kv-head; the CTA runs
+// two consecutive q-tiles (A, B) against every K/V tile it stages, so each
+// staged byte feeds 256 rows.  Key tiles are 128 keys = 128/B_p pages, each
+// page half (64 dims) fetched by one tiled TMA load straight from the pool
+// through the block table.
 //
-// Roles (192 threads):
-//   warp 0  TMA producer: Q tile once, then K tiles into a 3-stage ring
-//           (a stage frees when its S MMA completes) and V tiles into a
-//           2-stage ring (freed when its P*V MMA completes), issuing
-//           whichever load has a free stage.
-//   warp 1  MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
-//           buffers, then O += P_{j-1} V_{j-1} once the softmax published
-//           P_{j-1}; tcgen05.commit signals completion on mbarriers.
-//   warps 2-5  softmax: thread r owns row r (TMEM lane r): loads S_j, masks,
-//           online softmax in base 2 with lazy rescaling of O (only when the
-//           row max grows by more than 2^8), converts its key row of the V
-//           tile from bf16 to fp16 in place, writes P_j as fp16 into a
-//           128-byte-swizzled K-major tile, and finally normalises O.
+// Roles (384 threads, one CTA per SM):
+//   warp 0      TMA producer: both Q tiles once; K tiles into a 3-stage ring
+//               (a stage frees when the S MMAs of both q-tiles complete) and
+//               V tiles into a 2-stage ring (freed when both P*V MMAs
+//               complete).  Lane k handles page k of a tile.
+//   warp 1      MMA issuer (one thread): S_X = Q_X K_j^T into TMEM, then
+//               O_X += P_X V_j with P_X read from TMEM, alternating A and B so
+//               one q-tile's softmax overlaps the other's MMAs.
+//   warps 2-3   V converters: each K/V tile's V is turned from bf16 into fp16
+//               in place (rows past the written keys become zeros).
+//   warps 4-7   softmax of q-tile A, warps 8-11 softmax of q-tile B: thread r
+//               owns row r (TMEM lane r): two passes over S_j in TMEM (row max,
+//               then exponentials), base-2 online softmax with lazy rescaling
+//               of O (only when the row max grows by more than 2^8), P_j
+//               written as fp16 pairs into TMEM over the S columns already
+//               read, and finally O / l to global memory.
 // Q K^T runs on bf16 operands; P V runs on fp16 operands: P in [0, 2^8]
 // keeps 11 significant bits in fp16 against 8 in bf16, which the stated
 // accuracy needs (bf16 P alone leaves ~1.6e-3 relative L2 error at 2.5K
@@ -36,7 +40,6 @@
 // and the CTA winds down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
-#include <cuda_bf16.h>
 
 #include <cmath>
 #include <mutex>
@@ -47,24 +50,23 @@
 
 namespace pa {
 
-constexpr int kPfRows = 128;            // M: rows of a tile (queries x heads)
+constexpr int kPfRows = 128;            // M: rows of a q-tile (queries x heads)
 constexpr int kPfKeys = 128;            // N: keys per KV tile
 constexpr int kPfDim = 128;             // head_dim
-constexpr int kHalf = 128 * 128;        // bytes of one 64-column half of a 128-row bf16 tile
+constexpr int kHalf = 128 * 128;        // bytes of one 64-column half of a 128-row 16-bit tile
 constexpr int kTile = 2 * kHalf;        // 32 KiB
-constexpr int kPfThreads = 192;
-constexpr uint32_t kTmemCols = 512;     // S0 | S1 | O (| unused)
+constexpr int kPfThreads = 384;
+constexpr uint32_t kTmemCols = 512;     // S_A | S_B | O_A | O_B
 constexpr float kPfRescale = 8.0f;
 
 // shared-memory map (offsets from a 1024-aligned base)
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
-constexpr int kOffQ = 0;
-constexpr int kOffK = kTile;                         // kKStages stages
+constexpr int kOffQ = 0;                             // Q_A, Q_B
+constexpr int kOffK = 2 * kTile;                     // kKStages stages
 constexpr int kOffV = kOffK + kKStages * kTile;      // kVStages stages
-constexpr int kOffP = kOffV + kVStages * kTile;
-constexpr int kOffBar = kOffP + kTile;
-constexpr int kPfSmem = kOffBar + 1024 + 1024;  // + barriers and page ids, + alignment slack
+constexpr int kOffBar = kOffV + kVStages * kTile;
+constexpr int kPfSmem = kOffBar + 1024 + 1024;       // + barriers and page ids, + alignment slack
 
 struct PrefillParams {
     const int32_t* cu_seqlens_q;
@@ -82,7 +84,7 @@ struct PrefillParams {
     int32_t* d_err;
 };
 
-constexpr int kIdRing = 4;  // tiles of page ids kept for the V loads (K runs <= 3 tiles ahead)
+constexpr int kIdRing = 4;  // tiles of page ids kept for the V loads (K leads by <= 3)
 
 struct PfBars {
     int32_t page_row[kIdRing][32];  // pool row of each page of a tile (128 / B_p <= 16 used)
@@ -91,13 +93,25 @@ struct PfBars {
     uint64_t k_empty[kKStages];
     uint64_t v_full[kVStages];
     uint64_t v_empty[kVStages];
-    uint64_t s_full[2];
-    uint64_t s_empty[2];
-    uint64_t p_full;
-    uint64_t o_done;
+    uint64_t v_ready[kVStages];     // V converted to fp16 (64 converter threads)
+    uint64_t s_full[2];             // per q-tile: S_j in TMEM
+    uint64_t p_full[2];             // per q-tile: P_j in TMEM (128 softmax threads)
+    uint64_t o_done[2];             // per q-tile: P_j V_j accumulated into O
     uint32_t tmem_base;
     int32_t abort;
 };
+
+PA_DEVICE void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+PA_DEVICE uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
 
 // two floats -> fp16 pair (lo in the low half)
 PA_DEVICE uint32_t pack_f16(float lo, float hi) {
@@ -122,16 +136,24 @@ PA_DEVICE float add_f16x2_to(float acc, uint32_t h2) {
     return r;
 }
 
-PA_DEVICE uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
+// O (TMEM) += A (TMEM, fp16 pairs) * B (shared-memory descriptor)
+PA_DEVICE void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                      uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
-PA_DEVICE void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                 ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+PA_DEVICE void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+          "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+          "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
 }
 
 // bounded wait that also honours a CTA-wide abort flag
@@ -152,18 +174,25 @@ PA_DEVICE bool pf_wait(uint64_t* bar, uint32_t parity, PfBars* b, int32_t* d_err
     return true;
 }
 
+// A warp-uniform bounded wait (all lanes wait; the result is agreed by vote).
+PA_DEVICE bool pf_wait_warp(uint64_t* bar, uint32_t parity, PfBars* b, int32_t* d_err) {
+    const bool ok = pf_wait(bar, parity, b, d_err);
+    return __all_sync(0xffffffffu, ok);
+}
+
 template <int G>
 __global__ void __launch_bounds__(kPfThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
-    constexpr int QT = kPfRows / G;  // queries per tile
-    const int qt = p.max_qtiles - 1 - (int)blockIdx.x;  // longest tiles first
+    constexpr int QT = kPfRows / G;  // queries per q-tile
+    const int n_pairs = (p.max_qtiles + 1) / 2;
+    const int qp = n_pairs - 1 - (int)blockIdx.x;  // longest tiles first
     const int h = blockIdx.y, s = blockIdx.z;
     const int q_begin = __ldg(p.cu_seqlens_q + s);
     const int n_new = __ldg(p.cu_seqlens_q + s + 1) - q_begin;
-    const int q0 = qt * QT;
+    const int q0 = 2 * qp * QT;  // first query of q-tile A; q-tile B starts at q0 + QT
     if (n_new <= 0 || q0 >= n_new) {
-        if (qt == 0 && h == 0 && threadIdx.x == 0 && n_new > p.max_qtiles * QT)
+        if (qp == 0 && h == 0 && threadIdx.x == 0 && n_new > p.max_qtiles * QT)
             set_error(p.d_err, PA_ERR_OUT_OF_RANGE);
         return;
     }
@@ -173,9 +202,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         if (threadIdx.x == 0) set_error(p.d_err, PA_ERR_INVALID_ARG);
         return;
     }
-    const int q_last = min(q0 + QT, n_new) - 1;
-    const int kv_end = p.causal ? base_pos + q_last + 1 : ctx;  // keys [0, kv_end)
-    const int n_tiles = (kv_end + kPfKeys - 1) / kPfKeys;
+    const bool has_b = q0 + QT < n_new;
+    // keys each q-tile needs: [0, kv_end_X)
+    const int last_a = min(q0 + QT, n_new) - 1, last_b = min(q0 + 2 * QT, n_new) - 1;
+    const int kv_end_a = p.causal ? base_pos + last_a + 1 : ctx;
+    const int kv_end_b = has_b ? (p.causal ? base_pos + last_b + 1 : ctx) : 0;
+    const int kv_end = max(kv_end_a, kv_end_b);
+    const int nt_a = (kv_end_a + kPfKeys - 1) / kPfKeys;
+    const int nt_b = (kv_end_b + kPfKeys - 1) / kPfKeys;
+    const int n_tiles = max(nt_a, nt_b);
     const int bp = 1 << p.log2_bp;
     const int pages_per_tile = kPfKeys >> p.log2_bp;
     // keys at or past `zlim` may be unwritten or not loaded: V rows there are zeroed
@@ -196,13 +231,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         for (int i = 0; i < kVStages; ++i) {
             mbar_init(&bars->v_full[i], 1);
             mbar_init(&bars->v_empty[i], 1);
+            mbar_init(&bars->v_ready[i], 64);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->s_empty[i], 128);
+            mbar_init(&bars->p_full[i], 128);
+            mbar_init(&bars->o_done[i], 1);
         }
-        mbar_init(&bars->p_full, 128);
-        mbar_init(&bars->o_done, 1);
         bars->abort = 0;
         fence_mbar_init();
     }
@@ -214,14 +249,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
-    const uint32_t tS = tmem;             // columns [0, 256): two S buffers
-    const uint32_t tO = tmem + 256;       // columns [256, 384): O
+    // per q-tile X: S_X at columns [128 X, 128 X + 128); P_X (fp16 pairs) over its
+    // first 64 columns; O_X at [256 + 128 X, 256 + 128 X + 128)
+    auto tS = [&](int x) { return tmem + 128u * x; };
+    auto tO = [&](int x) { return tmem + 256u + 128u * x; };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        // The whole warp works: lane k handles page k of a tile (one coalesced
-        // table load per tile, prefetched a tile ahead, then its own TMA loads);
-        // lane 0 arms the barriers and decides when a stage is free.
         const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks;
         auto load_rows = [&](int j) -> int32_t {  // this lane's page of tile j
             const int e = j * pages_per_tile + lane;
@@ -241,9 +275,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             tc::prefetch_tmap(&tmap_q);
             tc::prefetch_tmap(&tmap_k);
             tc::prefetch_tmap(&tmap_v);
-            mbar_arrive_expect_tx(&bars->q_full, kTile);
+            mbar_arrive_expect_tx(&bars->q_full, has_b ? 2 * kTile : kTile);
             tc::tma_load_3d(smem + kOffQ, &tmap_q, 0, h * G, q_begin + q0, &bars->q_full);
             tc::tma_load_3d(smem + kOffQ + kHalf, &tmap_q, 64, h * G, q_begin + q0, &bars->q_full);
+            if (has_b) {
+                tc::tma_load_3d(smem + kOffQ + kTile, &tmap_q, 0, h * G, q_begin + q0 + QT,
+                                &bars->q_full);
+                tc::tma_load_3d(smem + kOffQ + kTile + kHalf, &tmap_q, 64, h * G,
+                                q_begin + q0 + QT, &bars->q_full);
+            }
         }
         int32_t next_row = load_rows(0);  // prefetched ids of tile kn
         int kn = 0, vn = 0;
@@ -251,7 +291,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         uint32_t spins = 0;
         while (kn < n_tiles || vn < n_tiles) {
             bool moved = false;
-            // K tile kn into its stage once the S MMA of tile kn - 3 has completed
             int go = 0;
             if (lane == 0)
                 go = kn < n_tiles && kn < vn + kIdRing &&  // page ids of tiles vn..kn stay live
@@ -273,7 +312,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 ++kn;
                 moved = true;
             }
-            // V tile vn once the P*V MMA of tile vn - 2 has completed
             go = 0;
             if (lane == 0)
                 go = vn < n_tiles && vn < kn &&
@@ -318,139 +356,84 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, 128, 0, 0);
             constexpr uint32_t idesc_pv = tc::idesc_f16_f32(128, 128, 0, 1);
             const uint32_t q_addr = smem_u32(smem + kOffQ);
-            const uint32_t p_addr = smem_u32(smem + kOffP);
+            const int nt[2] = {nt_a, nt_b};
             bool ok = pf_wait(&bars->q_full, 0, bars, p.d_err);
-            auto pv = [&](int t) -> bool {
-                if (!pf_wait(&bars->p_full, t & 1, bars, p.d_err)) return false;
-                tc::fence_after_sync();
-                const uint32_t v_addr = smem_u32(smem + kOffV + (t % kVStages) * kTile);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    const uint64_t b = tc::smem_desc_sw128(v_addr + kk * 2048, kHalf, 1024);
-                    tc::mma_bf16(tO, tc::smem_desc_sw128(p_addr + poff, 16, 1024), b, idesc_pv,
-                                 (t > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc::commit(&bars->o_done);
-                tc::commit(&bars->v_empty[t % kVStages]);
-                return true;
-            };
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const int st = j & 1;
-                const int ks = j % kKStages;
-                if (!pf_wait(&bars->k_full[ks], (j / kKStages) & 1, bars, p.d_err)) { ok = false; break; }
-                if (j >= 2 && !pf_wait(&bars->s_empty[st], ((j >> 1) - 1) & 1, bars, p.d_err)) { ok = false; break; }
-                tc::fence_after_sync();
-                const uint32_t k_addr = smem_u32(smem + kOffK + ks * kTile);
+            // S_X(j) = Q_X K_j^T
+            auto qk = [&](int x, int j) {
+                const uint32_t k_addr = smem_u32(smem + kOffK + (j % kKStages) * kTile);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    const uint64_t a = tc::smem_desc_sw128(q_addr + koff, 16, 1024);
-                    const uint64_t b = tc::smem_desc_sw128(k_addr + koff, 16, 1024);
-                    tc::mma_bf16(tS + st * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+                    tc::mma_bf16(tS(x), tc::smem_desc_sw128(q_addr + x * kTile + koff, 16, 1024),
+                                 tc::smem_desc_sw128(k_addr + koff, 16, 1024), idesc_qk,
+                                 kk > 0 ? 1u : 0u);
                 }
-                tc::commit(&bars->s_full[st]);
-                tc::commit(&bars->k_empty[ks]);
-                if (j >= 1 && !pv(j - 1)) { ok = false; break; }
+                tc::commit(&bars->s_full[x]);
+            };
+            // O_X += P_X(j) V_j, P_X in TMEM (8 columns of fp16 pairs per 16 keys)
+            auto pv = [&](int x, int j) {
+                const uint32_t v_addr = smem_u32(smem + kOffV + (j % kVStages) * kTile);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tO(x), tS(x) + kk * 8, tc::smem_desc_sw128(v_addr + kk * 2048, kHalf, 1024),
+                           idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                tc::commit(&bars->o_done[x]);
+            };
+            if (ok) ok = pf_wait(&bars->k_full[0], 0, bars, p.d_err);
+            if (ok) {
+                tc::fence_after_sync();
+                for (int x = 0; x < 2; ++x)
+                    if (nt[x] > 0) qk(x, 0);
+                tc::commit(&bars->k_empty[0]);
             }
-            if (ok) pv(n_tiles - 1);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const bool more = j + 1 < n_tiles;
+                bool k_next = false;
+                if (!pf_wait(&bars->v_ready[j % kVStages], (j / kVStages) & 1, bars, p.d_err)) {
+                    ok = false;
+                    break;
+                }
+                for (int x = 0; x < 2; ++x) {
+                    if (j >= nt[x]) continue;
+                    // P_X(j) published by its softmax (which read S_X(j) first)
+                    if (!pf_wait(&bars->p_full[x], j & 1, bars, p.d_err)) { ok = false; break; }
+                    tc::fence_after_sync();
+                    pv(x, j);
+                    if (j + 1 < nt[x]) {
+                        if (!k_next) {
+                            if (!pf_wait(&bars->k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1,
+                                         bars, p.d_err)) { ok = false; break; }
+                            tc::fence_after_sync();
+                            k_next = true;
+                        }
+                        qk(x, j + 1);  // overwrites P_X(j) after the P*V above consumed it
+                    }
+                }
+                if (!ok) break;
+                tc::commit(&bars->v_empty[j % kVStages]);
+                if (more) {
+                    if (!k_next) {  // neither q-tile uses K_{j+1}: still release its stage
+                        if (!pf_wait(&bars->k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1,
+                                     bars, p.d_err)) { ok = false; break; }
+                    }
+                    tc::commit(&bars->k_empty[(j + 1) % kKStages]);
+                }
+            }
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------------ softmax
-        const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;        // tile row == TMEM lane
-        const int i = r / G, g = r - i * G;
-        const int qi = q0 + i;
-        const bool live = qi < n_new;
-        int lim = p.causal ? base_pos + qi : ctx - 1;  // last visible key
-        if (!live) lim = 0;
-        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-        const uint32_t p_row = smem_u32(smem + kOffP) + r * 128;
-        float m_used = -INFINITY, l = 0.f;
-        bool ok = true;
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ V converters
+        const int t = (warp - 2) * 32 + lane;  // rows t and t + 64 of every V tile
         for (int j = 0; j < n_tiles; ++j) {
-            const int sb = j & 1;
-            ok = pf_wait(&bars->s_full[sb], (j >> 1) & 1, bars, p.d_err);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            tc::fence_after_sync();
-            uint32_t sr[4][32];
+            if (!pf_wait_warp(&bars->v_full[j % kVStages], (j / kVStages) & 1, bars, p.d_err)) break;
+            const uint32_t vbase = smem_u32(smem + kOffV + (j % kVStages) * kTile);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tc::tmem_ld32(tS + lane_addr + sb * 128 + c * 32, sr[c]);
-            tc::tmem_wait_ld();
-            tc::fence_before_sync();
-            mbar_arrive(&bars->s_empty[sb]);
-
-            const int key0 = j * kPfKeys;
-            float tmax = -INFINITY;
-            const bool full = key0 + kPfKeys - 1 <= lim;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float x = __uint_as_float(sr[c][e]) * p.scale_log2;
-                    if (!full && key0 + c * 32 + e > lim) x = -INFINITY;
-                    sr[c][e] = __float_as_uint(x);
-                    tmax = fmaxf(tmax, x);
-                }
-            bool o_ready = false;
-            if (j == 0) {
-                m_used = tmax;
-            } else {
-                const float m_new = fmaxf(m_used, tmax);
-                const bool need = m_new > m_used + kPfRescale;
-                if (__any_sync(0xffffffffu, need)) {
-                    // O holds tiles < j at scale m_used: wait for PV_{j-1}, then rescale
-                    ok = pf_wait(&bars->o_done, (j - 1) & 1, bars, p.d_err);
-                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                    o_ready = true;
-                    tc::fence_after_sync();
-                    const float f = need ? ex2(m_used - m_new) : 1.f;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t o[32];
-                        tc::tmem_ld32(tO + lane_addr + c * 32, o);
-                        tc::tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                        tc::tmem_st32(tO + lane_addr + c * 32, o);
-                    }
-                    tc::tmem_wait_st();
-                    tc::fence_before_sync();
-                    l *= f;
-                    if (need) m_used = m_new;
-                }
-            }
-            // probabilities (masked keys give exactly 0)
-            // probabilities in fp16; the row sum adds the rounded values the
-            // tensor cores multiply with
-            float lsum = 0.f;
-            uint32_t pk[64];
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float a = ex2(__uint_as_float(sr[c][e]) - m_used);
-                    const float b2 = ex2(__uint_as_float(sr[c][e + 1]) - m_used);
-                    const uint32_t w = pack_f16(a, b2);
-                    lsum = add_f16x2_to(lsum, w);
-                    pk[(c * 32 + e) >> 1] = w;
-                }
-            l += lsum;
-            // the P tile is single-buffered: PV_{j-1} must have finished reading it
-            if (j >= 1 && !o_ready) {
-                ok = pf_wait(&bars->o_done, (j - 1) & 1, bars, p.d_err);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            }
-            // this thread's key row of V_j: bf16 -> fp16 in place (16-byte chunks keep
-            // their swizzled positions); rows past the written keys become zeros
-            ok = pf_wait(&bars->v_full[j % kVStages], (j / kVStages) & 1, bars, p.d_err);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            {
-                const uint32_t vrow = smem_u32(smem + kOffV + (j % kVStages) * kTile) + r * 128;
-                // chunk order rotated by the row so the 8 threads of a 128-bit access
-                // phase touch 8 different bank groups
-                if (key0 + r < zlim) {
+            for (int half_row = 0; half_row < 2; ++half_row) {
+                const int r = t + 64 * half_row;
+                const uint32_t vrow = vbase + r * 128;
+                if (j * kPfKeys + r < zlim) {
+                    // chunk order rotated by the row: 8 threads of a 128-bit phase hit
+                    // 8 different bank groups
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
                         const uint32_t a = vrow + (c >> 3) * kHalf + ((c + r) & 7) * 16;
@@ -464,25 +447,110 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                         st_shared_v4(vrow + (c >> 3) * kHalf + ((c + r) & 7) * 16, 0, 0, 0, 0);
                 }
             }
-            // P row r: 16-byte chunk c (keys 8c..8c+7) at chunk (c mod 8) ^ (r mod 8) of half c/8
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint32_t addr = p_row + (c >> 3) * kHalf + (((c & 7) ^ (r & 7)) << 4);
-                st_shared_v4(addr, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            }
             fence_proxy_async_smem();
-            mbar_arrive(&bars->p_full);
+            mbar_arrive(&bars->v_ready[j % kVStages]);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int x = warp >= 8 ? 1 : 0;           // q-tile A or B
+        const int nt_x = x ? nt_b : nt_a;
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;         // tile row == TMEM lane
+        const int i = r / G, g = r - i * G;
+        const int qi = q0 + x * QT + i;
+        const bool live = qi < n_new;
+        int lim = p.causal ? base_pos + qi : ctx - 1;  // last visible key
+        if (!live) lim = 0;
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        const uint32_t sX = tS(x) + lane_addr, oX = tO(x) + lane_addr;
+        const float sc = p.scale_log2;
+        float m_used = -INFINITY, l = 0.f;  // m_used in scaled base-2 units
+        bool ok = true;
+        for (int j = 0; j < nt_x; ++j) {
+            if (!pf_wait_warp(&bars->s_full[x], j & 1, bars, p.d_err)) { ok = false; break; }
+            tc::fence_after_sync();
+            const int key0 = j * kPfKeys;
+            const bool full = key0 + kPfKeys - 1 <= lim;
+            // pass 1: row max of the raw scores over the visible keys
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; c += 2) {
+                uint32_t a[32], b[32];
+                tc::tmem_ld32(sX + c * 32, a);
+                tc::tmem_ld32(sX + (c + 1) * 32, b);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float va = __uint_as_float(a[e]), vb = __uint_as_float(b[e]);
+                    tmax = fmaxf(tmax, (full || key0 + c * 32 + e <= lim) ? va : -INFINITY);
+                    tmax = fmaxf(tmax, (full || key0 + (c + 1) * 32 + e <= lim) ? vb : -INFINITY);
+                }
+            }
+            const float tmax_s = tmax * sc;
+            if (j == 0) {
+                m_used = tmax_s;
+            } else {
+                const float m_new = fmaxf(m_used, tmax_s);
+                const bool need = m_new > m_used + kPfRescale;
+                if (__any_sync(0xffffffffu, need)) {
+                    // O holds tiles < j at scale m_used: wait for P_{j-1} V_{j-1}, rescale
+                    if (!pf_wait_warp(&bars->o_done[x], (j - 1) & 1, bars, p.d_err)) { ok = false; break; }
+                    tc::fence_after_sync();
+                    const float f = need ? ex2(m_used - m_new) : 1.f;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tc::tmem_ld32(oX + c * 32, o);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                        tc::tmem_st32(oX + c * 32, o);
+                    }
+                    tc::tmem_wait_st();
+                    l *= f;
+                    if (need) m_used = m_new;
+                }
+            }
+            // pass 2: P = 2^(s*scale - m) as fp16 pairs, written over the S columns
+            // already read (chunk c of 32 scores -> columns 16c..16c+15)
+            const float neg_m = -m_used;
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t a[32];
+                tc::tmem_ld32(sX + c * 32, a);
+                tc::tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int k = key0 + c * 32 + e;
+                    float v0 = fmaf(__uint_as_float(a[e]), sc, neg_m);
+                    float v1 = fmaf(__uint_as_float(a[e + 1]), sc, neg_m);
+                    if (!full) {
+                        if (k > lim) v0 = -INFINITY;
+                        if (k + 1 > lim) v1 = -INFINITY;
+                    }
+                    const uint32_t w = pack_f16(ex2(v0), ex2(v1));
+                    lsum = add_f16x2_to(lsum, w);
+                    pk[e >> 1] = w;
+                }
+                tmem_st16(sX + c * 16, pk);
+            }
+            tc::tmem_wait_st();
+            l += lsum;
+            tc::fence_before_sync();
+            mbar_arrive(&bars->p_full[x]);
         }
         // epilogue: O / l -> out
-        if (ok) ok = pf_wait(&bars->o_done, (n_tiles - 1) & 1, bars, p.d_err);
-        if (__all_sync(0xffffffffu, ok)) {
+        if (ok && nt_x > 0) ok = pf_wait_warp(&bars->o_done[x], (nt_x - 1) & 1, bars, p.d_err);
+        if (ok && nt_x > 0) {
             tc::fence_after_sync();
             const float inv = live ? 1.f / l : 0.f;
             float* orow = p.out + ((int64_t)(q_begin + qi) * p.num_q_heads + h * G + g) * kPfDim;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t o[32];
-                tc::tmem_ld32(tO + lane_addr + c * 32, o);
+                tc::tmem_ld32(oX + c * 32, o);
                 tc::tmem_wait_ld();
                 if (live) {
 #pragma unroll
@@ -557,7 +625,7 @@ static pa_status launch_prefill(const pa_kv_pool* pool, const void* q, int32_t t
         }
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
-    dim3 grid((unsigned)prm.max_qtiles, (unsigned)pool->num_kv_heads, (unsigned)B);
+    dim3 grid((unsigned)((prm.max_qtiles + 1) / 2), (unsigned)pool->num_kv_heads, (unsigned)B);
     kern<<<grid, kPfThreads, kPfSmem, stream>>>(mq, mk, mv, prm);
     return launch_status();
 }
