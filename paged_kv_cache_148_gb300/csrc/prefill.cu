@@ -136,6 +136,20 @@ PA_DEVICE float add_f16x2_to(float acc, uint32_t h2) {
     return r;
 }
 
+// an fp16 pair times a float, back to an fp16 pair
+PA_DEVICE uint32_t scale_f16x2(uint32_t h2, float f) {
+    float lo, hi;
+    asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b; }"
+        : "=f"(lo), "=f"(hi) : "r"(h2));
+    return pack_f16(lo * f, hi * f);
+}
+
+PA_DEVICE float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // O (TMEM) += A (TMEM, fp16 pairs) * B (shared-memory descriptor)
 PA_DEVICE void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                       uint32_t accumulate) {
@@ -466,37 +480,90 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         const float sc = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;  // m_used in scaled base-2 units
         bool ok = true;
+        // P for half `hf` of the tile (scores 64 hf .. 64 hf + 63, two TMEM chunks
+        // loaded with one wait) against the running max: fp16 pairs into pk,
+        // the fp32 sum into lsum.  Masked keys give exactly 0.  Returns the
+        // largest scaled score minus m_used (-inf if none is visible).
+        auto p_half = [&](int hf, int key0, bool full, uint32_t (&pk)[32], float& lsum) {
+            uint32_t a[32], b[32];
+            tc::tmem_ld32(sX + (2 * hf) * 32, a);
+            tc::tmem_ld32(sX + (2 * hf + 1) * 32, b);
+            tc::tmem_wait_ld();
+            const float neg_m = -m_used;
+            float vmax = -INFINITY;
+            lsum = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t* src = hh ? b : a;
+                const int kbase = key0 + (2 * hf + hh) * 32;
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float v0 = fmaf(__uint_as_float(src[e]), sc, neg_m);
+                    float v1 = fmaf(__uint_as_float(src[e + 1]), sc, neg_m);
+                    if (!full) {
+                        if (kbase + e > lim) v0 = -INFINITY;
+                        if (kbase + e + 1 > lim) v1 = -INFINITY;
+                    }
+                    vmax = fmax3(vmax, v0, v1);
+                    const float p0 = ex2(v0), p1 = ex2(v1);
+                    lsum += p0 + p1;
+                    pk[hh * 16 + (e >> 1)] = pack_f16(p0, p1);
+                }
+            }
+            return vmax;
+        };
         for (int j = 0; j < nt_x; ++j) {
             if (!pf_wait_warp(&bars->s_full[x], j & 1, bars, p.d_err)) { ok = false; break; }
             tc::fence_after_sync();
             const int key0 = j * kPfKeys;
             const bool full = key0 + kPfKeys - 1 <= lim;
-            // pass 1: row max of the raw scores over the visible keys
-            float tmax = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 4; c += 2) {
-                uint32_t a[32], b[32];
-                tc::tmem_ld32(sX + c * 32, a);
-                tc::tmem_ld32(sX + (c + 1) * 32, b);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float va = __uint_as_float(a[e]), vb = __uint_as_float(b[e]);
-                    tmax = fmaxf(tmax, (full || key0 + c * 32 + e <= lim) ? va : -INFINITY);
-                    tmax = fmaxf(tmax, (full || key0 + (c + 1) * 32 + e <= lim) ? vb : -INFINITY);
-                }
-            }
-            const float tmax_s = tmax * sc;
             if (j == 0) {
-                m_used = tmax_s;
-            } else {
-                const float m_new = fmaxf(m_used, tmax_s);
-                const bool need = m_new > m_used + kPfRescale;
-                if (__any_sync(0xffffffffu, need)) {
-                    // O holds tiles < j at scale m_used: wait for P_{j-1} V_{j-1}, rescale
-                    if (!pf_wait_warp(&bars->o_done[x], (j - 1) & 1, bars, p.d_err)) { ok = false; break; }
-                    tc::fence_after_sync();
-                    const float f = need ? ex2(m_used - m_new) : 1.f;
+                // first tile: the row max comes first (no running max yet)
+                float tmax = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; c += 2) {
+                    uint32_t a[32], b[32];
+                    tc::tmem_ld32(sX + c * 32, a);
+                    tc::tmem_ld32(sX + (c + 1) * 32, b);
+                    tc::tmem_wait_ld();
+                    if (full) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            tmax = fmax3(tmax, __uint_as_float(a[e]), __uint_as_float(b[e]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const bool va = key0 + c * 32 + e <= lim;
+                            const bool vb = key0 + (c + 1) * 32 + e <= lim;
+                            tmax = fmax3(tmax, va ? __uint_as_float(a[e]) : -INFINITY,
+                                         vb ? __uint_as_float(b[e]) : -INFINITY);
+                        }
+                    }
+                }
+                m_used = tmax * sc;
+            }
+            // One pass per half against the running max.  If a score exceeds it by
+            // more than 2^8 (rare after the first tile): rescale O, l and the P half
+            // already stored, then redo this half (its S columns are still intact:
+            // P of half h is stored over S columns 32 h .. 32 h + 31, scores that
+            // half h has already read).
+            float l_tile = 0.f;
+            bool o_waited = false;
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t pk[32];
+                float lsum;
+                float vmax = p_half(hf, key0, full, pk, lsum);
+                const bool need = vmax > kPfRescale;
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                    if (!o_waited) {
+                        // O holds tiles < j: wait for P_{j-1} V_{j-1} before touching it
+                        if (!pf_wait_warp(&bars->o_done[x], (j - 1) & 1, bars, p.d_err)) { ok = false; break; }
+                        tc::fence_after_sync();
+                        o_waited = true;
+                    }
+                    const float m_new = need ? m_used + vmax : m_used;
+                    const float f = ex2(m_used - m_new);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t o[32];
@@ -506,38 +573,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
                         tc::tmem_st32(oX + c * 32, o);
                     }
+                    if (hf == 1) {
+                        // first half of P (columns 0..31, fp16 pairs) to the new scale
+                        uint32_t q[32];
+                        tc::tmem_ld32(sX, q);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) q[e] = scale_f16x2(q[e], f);
+                        tc::tmem_st32(sX, q);
+                    }
                     tc::tmem_wait_st();
                     l *= f;
-                    if (need) m_used = m_new;
+                    l_tile *= f;
+                    m_used = m_new;
+                    p_half(hf, key0, full, pk, lsum);
                 }
+                tmem_st16(sX + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(pk));
+                tmem_st16(sX + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
+                l_tile += lsum;
             }
-            // pass 2: P = 2^(s*scale - m) as fp16 pairs, written over the S columns
-            // already read (chunk c of 32 scores -> columns 16c..16c+15)
-            const float neg_m = -m_used;
-            float lsum = 0.f;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t a[32];
-                tc::tmem_ld32(sX + c * 32, a);
-                tc::tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const int k = key0 + c * 32 + e;
-                    float v0 = fmaf(__uint_as_float(a[e]), sc, neg_m);
-                    float v1 = fmaf(__uint_as_float(a[e + 1]), sc, neg_m);
-                    if (!full) {
-                        if (k > lim) v0 = -INFINITY;
-                        if (k + 1 > lim) v1 = -INFINITY;
-                    }
-                    const uint32_t w = pack_f16(ex2(v0), ex2(v1));
-                    lsum = add_f16x2_to(lsum, w);
-                    pk[e >> 1] = w;
-                }
-                tmem_st16(sX + c * 16, pk);
-            }
+            if (!ok) break;
             tc::tmem_wait_st();
-            l += lsum;
+            l += l_tile;
             tc::fence_before_sync();
             mbar_arrive(&bars->p_full[x]);
         }
