@@ -60,8 +60,8 @@ constexpr uint32_t kTmemCols = 512;     // S_A | S_B | O_A | O_B
 constexpr float kPfRescale = 8.0f;
 
 // shared-memory map (offsets from a 1024-aligned base)
-constexpr int kKStages = 3;
-constexpr int kVStages = 2;
+constexpr int kKStages = 2;
+constexpr int kVStages = 3;
 constexpr int kOffQ = 0;                             // Q_A, Q_B
 constexpr int kOffK = 2 * kTile;                     // kKStages stages
 constexpr int kOffV = kOffK + kKStages * kTile;      // kVStages stages
@@ -84,7 +84,7 @@ struct PrefillParams {
     int32_t* d_err;
 };
 
-constexpr int kIdRing = 4;  // tiles of page ids kept for the V loads (K leads by <= 3)
+constexpr int kIdRing = 4;  // tiles of page ids kept for the V loads
 
 struct PfBars {
     int32_t page_row[kIdRing][32];  // pool row of each page of a tile (128 / B_p <= 16 used)
@@ -95,7 +95,7 @@ struct PfBars {
     uint64_t v_empty[kVStages];
     uint64_t v_ready[kVStages];     // V converted to fp16 (64 converter threads)
     uint64_t s_full[2];             // per q-tile: S_j in TMEM
-    uint64_t p_full[2];             // per q-tile: P_j in TMEM (128 softmax threads)
+    uint64_t p_full[2][2];          // per q-tile and half of the keys: P_j in TMEM (128 threads)
     uint64_t o_done[2];             // per q-tile: P_j V_j accumulated into O
     uint32_t tmem_base;
     int32_t abort;
@@ -158,6 +158,16 @@ PA_DEVICE void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
         ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+PA_DEVICE void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
 }
 
 PA_DEVICE void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -249,7 +259,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->p_full[i], 128);
+            mbar_init(&bars->p_full[i][0], 128);
+            mbar_init(&bars->p_full[i][1], 128);
             mbar_init(&bars->o_done[i], 1);
         }
         bars->abort = 0;
@@ -384,14 +395,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 }
                 tc::commit(&bars->s_full[x]);
             };
-            // O_X += P_X(j) V_j, P_X in TMEM (8 columns of fp16 pairs per 16 keys)
-            auto pv = [&](int x, int j) {
+            // O_X += P_X(j) V_j, P_X in TMEM (8 columns of fp16 pairs per 16 keys);
+            // the softmax publishes P in two halves of 64 keys
+            auto pv = [&](int x, int j) -> bool {
                 const uint32_t v_addr = smem_u32(smem + kOffV + (j % kVStages) * kTile);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tO(x), tS(x) + kk * 8, tc::smem_desc_sw128(v_addr + kk * 2048, kHalf, 1024),
-                           idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                for (int hf = 0; hf < 2; ++hf) {
+                    if (!pf_wait(&bars->p_full[x][hf], j & 1, bars, p.d_err)) return false;
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 4 * hf; kk < 4 * hf + 4; ++kk)
+                        mma_ts(tO(x), tS(x) + kk * 8,
+                               tc::smem_desc_sw128(v_addr + kk * 2048, kHalf, 1024), idesc_pv,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                }
                 tc::commit(&bars->o_done[x]);
+                return true;
             };
             if (ok) ok = pf_wait(&bars->k_full[0], 0, bars, p.d_err);
             if (ok) {
@@ -410,9 +429,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 for (int x = 0; x < 2; ++x) {
                     if (j >= nt[x]) continue;
                     // P_X(j) published by its softmax (which read S_X(j) first)
-                    if (!pf_wait(&bars->p_full[x], j & 1, bars, p.d_err)) { ok = false; break; }
-                    tc::fence_after_sync();
-                    pv(x, j);
+                    if (!pv(x, j)) { ok = false; break; }
                     if (j + 1 < nt[x]) {
                         if (!k_next) {
                             if (!pf_wait(&bars->k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1,
@@ -480,123 +497,76 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         const float sc = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;  // m_used in scaled base-2 units
         bool ok = true;
-        // P for half `hf` of the tile (scores 64 hf .. 64 hf + 63, two TMEM chunks
-        // loaded with one wait) against the running max: fp16 pairs into pk,
-        // the fp32 sum into lsum.  Masked keys give exactly 0.  Returns the
-        // largest scaled score minus m_used (-inf if none is visible).
-        auto p_half = [&](int hf, int key0, bool full, uint32_t (&pk)[32], float& lsum) {
-            uint32_t a[32], b[32];
-            tc::tmem_ld32(sX + (2 * hf) * 32, a);
-            tc::tmem_ld32(sX + (2 * hf + 1) * 32, b);
-            tc::tmem_wait_ld();
-            const float neg_m = -m_used;
-            float vmax = -INFINITY;
-            lsum = 0.f;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const uint32_t* src = hh ? b : a;
-                const int kbase = key0 + (2 * hf + hh) * 32;
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float v0 = fmaf(__uint_as_float(src[e]), sc, neg_m);
-                    float v1 = fmaf(__uint_as_float(src[e + 1]), sc, neg_m);
-                    if (!full) {
-                        if (kbase + e > lim) v0 = -INFINITY;
-                        if (kbase + e + 1 > lim) v1 = -INFINITY;
-                    }
-                    vmax = fmax3(vmax, v0, v1);
-                    const float p0 = ex2(v0), p1 = ex2(v1);
-                    lsum += p0 + p1;
-                    pk[hh * 16 + (e >> 1)] = pack_f16(p0, p1);
-                }
-            }
-            return vmax;
-        };
         for (int j = 0; j < nt_x; ++j) {
             if (!pf_wait_warp(&bars->s_full[x], j & 1, bars, p.d_err)) { ok = false; break; }
             tc::fence_after_sync();
             const int key0 = j * kPfKeys;
             const bool full = key0 + kPfKeys - 1 <= lim;
-            if (j == 0) {
-                // first tile: the row max comes first (no running max yet)
-                float tmax = -INFINITY;
+            // the whole S row with one TMEM wait
+            uint32_t sr[4][32];
 #pragma unroll
-                for (int c = 0; c < 4; c += 2) {
-                    uint32_t a[32], b[32];
-                    tc::tmem_ld32(sX + c * 32, a);
-                    tc::tmem_ld32(sX + (c + 1) * 32, b);
-                    tc::tmem_wait_ld();
-                    if (full) {
+            for (int c = 0; c < 4; ++c) tc::tmem_ld32(sX + c * 32, sr[c]);
+            tc::tmem_wait_ld();
+            if (!full) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            tmax = fmax3(tmax, __uint_as_float(a[e]), __uint_as_float(b[e]));
-                    } else {
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const bool va = key0 + c * 32 + e <= lim;
-                            const bool vb = key0 + (c + 1) * 32 + e <= lim;
-                            tmax = fmax3(tmax, va ? __uint_as_float(a[e]) : -INFINITY,
-                                         vb ? __uint_as_float(b[e]) : -INFINITY);
-                        }
-                    }
-                }
-                m_used = tmax * sc;
+                    for (int e = 0; e < 32; ++e)
+                        if (key0 + c * 32 + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
             }
-            // One pass per half against the running max.  If a score exceeds it by
-            // more than 2^8 (rare after the first tile): rescale O, l and the P half
-            // already stored, then redo this half (its S columns are still intact:
-            // P of half h is stored over S columns 32 h .. 32 h + 31, scores that
-            // half h has already read).
-            float l_tile = 0.f;
-            bool o_waited = false;
-#pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t pk[32];
-                float lsum;
-                float vmax = p_half(hf, key0, full, pk, lsum);
-                const bool need = vmax > kPfRescale;
-                if (j > 0 && __any_sync(0xffffffffu, need)) {
-                    if (!o_waited) {
-                        // O holds tiles < j: wait for P_{j-1} V_{j-1} before touching it
-                        if (!pf_wait_warp(&bars->o_done[x], (j - 1) & 1, bars, p.d_err)) { ok = false; break; }
-                        tc::fence_after_sync();
-                        o_waited = true;
-                    }
-                    const float m_new = need ? m_used + vmax : m_used;
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; e += 2)
+                    tmax = fmax3(tmax, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+            const float tmax_s = tmax * sc;
+            if (j == 0) {
+                m_used = tmax_s;
+            } else {
+                // rescale O and l only when the row max grew by more than 2^8
+                const bool need = tmax_s > m_used + kPfRescale;
+                if (__any_sync(0xffffffffu, need)) {
+                    if (!pf_wait_warp(&bars->o_done[x], (j - 1) & 1, bars, p.d_err)) { ok = false; break; }
+                    tc::fence_after_sync();
+                    const float m_new = need ? tmax_s : m_used;
                     const float f = ex2(m_used - m_new);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t o[32];
-                        tc::tmem_ld32(oX + c * 32, o);
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {  // 16 columns at a time: S is still live
+                        uint32_t o[16];
+                        tmem_ld16(oX + c * 16, o);
                         tc::tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                        tc::tmem_st32(oX + c * 32, o);
-                    }
-                    if (hf == 1) {
-                        // first half of P (columns 0..31, fp16 pairs) to the new scale
-                        uint32_t q[32];
-                        tc::tmem_ld32(sX, q);
-                        tc::tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) q[e] = scale_f16x2(q[e], f);
-                        tc::tmem_st32(sX, q);
+                        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                        tmem_st16(oX + c * 16, o);
                     }
                     tc::tmem_wait_st();
                     l *= f;
-                    l_tile *= f;
                     m_used = m_new;
-                    p_half(hf, key0, full, pk, lsum);
                 }
-                tmem_st16(sX + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(pk));
-                tmem_st16(sX + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
-                l_tile += lsum;
             }
-            if (!ok) break;
-            tc::tmem_wait_st();
-            l += l_tile;
-            tc::fence_before_sync();
-            mbar_arrive(&bars->p_full[x]);
+            // P = 2^(s*scale - m) as fp16 pairs over the S columns already read;
+            // each half of 64 keys is published as soon as it is stored
+            const float neg_m = -m_used;
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float p0 = ex2(fmaf(__uint_as_float(sr[c][e]), sc, neg_m));
+                    const float p1 = ex2(fmaf(__uint_as_float(sr[c][e + 1]), sc, neg_m));
+                    lsum += p0 + p1;
+                    pk[e >> 1] = pack_f16(p0, p1);
+                }
+                tmem_st16(sX + c * 16, pk);
+                if (c & 1) {
+                    tc::tmem_wait_st();
+                    tc::fence_before_sync();
+                    mbar_arrive(&bars->p_full[x][c >> 1]);
+                }
+            }
+            l += lsum;
         }
         // epilogue: O / l -> out
         if (ok && nt_x > 0) ok = pf_wait_warp(&bars->o_done[x], (nt_x - 1) & 1, bars, p.d_err);
