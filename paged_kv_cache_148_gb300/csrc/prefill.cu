@@ -383,30 +383,35 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             const uint32_t q_addr = smem_u32(smem + kOffQ);
             const int nt[2] = {nt_a, nt_b};
             bool ok = pf_wait(&bars->q_full, 0, bars, p.d_err);
+            // Shared-memory descriptors are built once; an MMA step only adds the
+            // byte offset (>> 4) of its sub-tile to the start-address field.
+            const uint64_t dq = tc::smem_desc_sw128(q_addr, 16, 1024);
+            const uint64_t dk = tc::smem_desc_sw128(smem_u32(smem + kOffK), 16, 1024);
+            const uint64_t dv = tc::smem_desc_sw128(smem_u32(smem + kOffV), kHalf, 1024);
             // S_X(j) = Q_X K_j^T
             auto qk = [&](int x, int j) {
-                const uint32_t k_addr = smem_u32(smem + kOffK + (j % kKStages) * kTile);
+                const uint64_t a0 = dq + (uint64_t)((x * kTile) >> 4);
+                const uint64_t b0 = dk + (uint64_t)(((j % kKStages) * kTile) >> 4);
+                const uint32_t d = tS(x);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    tc::mma_bf16(tS(x), tc::smem_desc_sw128(q_addr + x * kTile + koff, 16, 1024),
-                                 tc::smem_desc_sw128(k_addr + koff, 16, 1024), idesc_qk,
-                                 kk > 0 ? 1u : 0u);
+                    const uint64_t koff = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+                    tc::mma_bf16(d, a0 + koff, b0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 tc::commit(&bars->s_full[x]);
             };
             // O_X += P_X(j) V_j, P_X in TMEM (8 columns of fp16 pairs per 16 keys);
             // the softmax publishes P in two halves of 64 keys
             auto pv = [&](int x, int j) -> bool {
-                const uint32_t v_addr = smem_u32(smem + kOffV + (j % kVStages) * kTile);
+                const uint64_t b0 = dv + (uint64_t)(((j % kVStages) * kTile) >> 4);
+                const uint32_t d = tO(x), a = tS(x);
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     if (!pf_wait(&bars->p_full[x][hf], j & 1, bars, p.d_err)) return false;
                     tc::fence_after_sync();
 #pragma unroll
                     for (int kk = 4 * hf; kk < 4 * hf + 4; ++kk)
-                        mma_ts(tO(x), tS(x) + kk * 8,
-                               tc::smem_desc_sw128(v_addr + kk * 2048, kHalf, 1024), idesc_pv,
+                        mma_ts(d, a + kk * 8, b0 + (uint64_t)((kk * 2048) >> 4), idesc_pv,
                                (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc::commit(&bars->o_done[x]);
@@ -514,12 +519,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     for (int e = 0; e < 32; ++e)
                         if (key0 + c * 32 + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
             }
-            float tmax = -INFINITY;
+            // row max as 8 independent chains (the 128 values are all in registers)
+            float mx[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) mx[q] = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int e = 0; e < 32; e += 2)
-                    tmax = fmax3(tmax, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+                for (int e = 0; e < 32; e += 2) {
+                    const int q = ((c * 32 + e) >> 1) & 7;
+                    mx[q] = fmax3(mx[q], __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+                }
+            const float tmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
             const float tmax_s = tmax * sc;
             if (j == 0) {
                 m_used = tmax_s;
@@ -548,7 +559,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             // P = 2^(s*scale - m) as fp16 pairs over the S columns already read;
             // each half of 64 keys is published as soon as it is stored
             const float neg_m = -m_used;
-            float lsum = 0.f;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16];
@@ -556,7 +567,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 for (int e = 0; e < 32; e += 2) {
                     const float p0 = ex2(fmaf(__uint_as_float(sr[c][e]), sc, neg_m));
                     const float p1 = ex2(fmaf(__uint_as_float(sr[c][e + 1]), sc, neg_m));
-                    lsum += p0 + p1;
+                    ls[(e >> 1) & 3] += p0 + p1;
                     pk[e >> 1] = pack_f16(p0, p1);
                 }
                 tmem_st16(sX + c * 16, pk);
@@ -566,7 +577,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     mbar_arrive(&bars->p_full[x][c >> 1]);
                 }
             }
-            l += lsum;
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
         // epilogue: O / l -> out
         if (ok && nt_x > 0) ok = pf_wait_warp(&bars->o_done[x], (nt_x - 1) & 1, bars, p.d_err);
