@@ -128,36 +128,10 @@ PA_DEVICE uint32_t bf16x2_to_f16x2(uint32_t w) {
     return r;
 }
 
-// acc + lo + hi of an fp16 pair, accumulated in fp32
-PA_DEVICE float add_f16x2_to(float acc, uint32_t h2) {
-    float r;
-    asm("{ .reg .b16 a, b; mov.b32 {a, b}, %1; add.rn.f32.f16 %0, a, %2; add.rn.f32.f16 %0, b, %0; }"
-        : "=f"(r) : "r"(h2), "f"(acc));
-    return r;
-}
-
-// an fp16 pair times a float, back to an fp16 pair
-PA_DEVICE uint32_t scale_f16x2(uint32_t h2, float f) {
-    float lo, hi;
-    asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b; }"
-        : "=f"(lo), "=f"(hi) : "r"(h2));
-    return pack_f16(lo * f, hi * f);
-}
-
 PA_DEVICE float fmax3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
-}
-
-// O (TMEM) += A (TMEM, fp16 pairs) * B (shared-memory descriptor)
-PA_DEVICE void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                      uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
 PA_DEVICE void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -377,83 +351,86 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, 128, 0, 0);
-            constexpr uint32_t idesc_pv = tc::idesc_f16_f32(128, 128, 0, 1);
-            const uint32_t q_addr = smem_u32(smem + kOffQ);
-            const int nt[2] = {nt_a, nt_b};
-            bool ok = pf_wait(&bars->q_full, 0, bars, p.d_err);
-            // Shared-memory descriptors are built once; an MMA step only adds the
-            // byte offset (>> 4) of its sub-tile to the start-address field.
-            const uint64_t dq = tc::smem_desc_sw128(q_addr, 16, 1024);
-            const uint64_t dk = tc::smem_desc_sw128(smem_u32(smem + kOffK), 16, 1024);
-            const uint64_t dv = tc::smem_desc_sw128(smem_u32(smem + kOffV), kHalf, 1024);
-            // S_X(j) = Q_X K_j^T
-            auto qk = [&](int x, int j) {
-                const uint64_t a0 = dq + (uint64_t)((x * kTile) >> 4);
-                const uint64_t b0 = dk + (uint64_t)(((j % kKStages) * kTile) >> 4);
-                const uint32_t d = tS(x);
+        // The whole warp runs the issue loop (waits are warp-wide votes) and one
+        // elected lane issues each tcgen05 instruction.
+        constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, 128, 0, 0);
+        constexpr uint32_t idesc_pv = tc::idesc_f16_f32(128, 128, 0, 1);
+        const uint32_t q_addr = smem_u32(smem + kOffQ);
+        const int nt[2] = {nt_a, nt_b};
+        bool ok = pf_wait_warp(&bars->q_full, 0, bars, p.d_err);
+        // Shared-memory descriptors are built once; an MMA step only adds the
+        // byte offset (>> 4) of its sub-tile to the start-address field.
+        const uint64_t dq = tc::smem_desc_sw128(q_addr, 16, 1024);
+        const uint64_t dk = tc::smem_desc_sw128(smem_u32(smem + kOffK), 16, 1024);
+        const uint64_t dv = tc::smem_desc_sw128(smem_u32(smem + kOffV), kHalf, 1024);
+        // S_X(j) = Q_X K_j^T
+        auto qk = [&](int x, int j) {
+            const uint64_t a0 = dq + (uint64_t)((x * kTile) >> 4);
+            const uint64_t b0 = dk + (uint64_t)(((j % kKStages) * kTile) >> 4);
+            const uint32_t d = tS(x);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t koff = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
-                    tc::mma_bf16(d, a0 + koff, b0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
-                }
-                tc::commit(&bars->s_full[x]);
-            };
-            // O_X += P_X(j) V_j, P_X in TMEM (8 columns of fp16 pairs per 16 keys);
-            // the softmax publishes P in two halves of 64 keys
-            auto pv = [&](int x, int j) -> bool {
-                const uint64_t b0 = dv + (uint64_t)(((j % kVStages) * kTile) >> 4);
-                const uint32_t d = tO(x), a = tS(x);
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    if (!pf_wait(&bars->p_full[x][hf], j & 1, bars, p.d_err)) return false;
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int kk = 4 * hf; kk < 4 * hf + 4; ++kk)
-                        mma_ts(d, a + kk * 8, b0 + (uint64_t)((kk * 2048) >> 4), idesc_pv,
-                               (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc::commit(&bars->o_done[x]);
-                return true;
-            };
-            if (ok) ok = pf_wait(&bars->k_full[0], 0, bars, p.d_err);
-            if (ok) {
-                tc::fence_after_sync();
-                for (int x = 0; x < 2; ++x)
-                    if (nt[x] > 0) qk(x, 0);
-                tc::commit(&bars->k_empty[0]);
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t koff = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+                tc::mma_ss_warp(d, a0 + koff, b0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
             }
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const bool more = j + 1 < n_tiles;
-                bool k_next = false;
-                if (!pf_wait(&bars->v_ready[j % kVStages], (j / kVStages) & 1, bars, p.d_err)) {
-                    ok = false;
-                    break;
-                }
-                for (int x = 0; x < 2; ++x) {
-                    if (j >= nt[x]) continue;
-                    // P_X(j) published by its softmax (which read S_X(j) first)
-                    if (!pv(x, j)) { ok = false; break; }
-                    if (j + 1 < nt[x]) {
-                        if (!k_next) {
-                            if (!pf_wait(&bars->k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1,
-                                         bars, p.d_err)) { ok = false; break; }
-                            tc::fence_after_sync();
-                            k_next = true;
+            tc::commit_warp(&bars->s_full[x]);
+        };
+        // O_X += P_X(j) V_j, P_X in TMEM (8 columns of fp16 pairs per 16 keys);
+        // the softmax publishes P in two halves of 64 keys
+        auto pv = [&](int x, int j) -> bool {
+            const uint64_t b0 = dv + (uint64_t)(((j % kVStages) * kTile) >> 4);
+            const uint32_t d = tO(x), a = tS(x);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                if (!pf_wait_warp(&bars->p_full[x][hf], j & 1, bars, p.d_err)) return false;
+                tc::fence_after_sync();
+#pragma unroll
+                for (int kk = 4 * hf; kk < 4 * hf + 4; ++kk)
+                    tc::mma_ts_warp(d, a + kk * 8, b0 + (uint64_t)((kk * 2048) >> 4), idesc_pv,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc::commit_warp(&bars->o_done[x]);
+            return true;
+        };
+        if (ok) ok = pf_wait_warp(&bars->k_full[0], 0, bars, p.d_err);
+        if (ok) {
+            tc::fence_after_sync();
+            for (int x = 0; x < 2; ++x)
+                if (nt[x] > 0) qk(x, 0);
+            tc::commit_warp(&bars->k_empty[0]);
+        }
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            const bool more = j + 1 < n_tiles;
+            bool k_next = false;
+            if (!pf_wait_warp(&bars->v_ready[j % kVStages], (j / kVStages) & 1, bars, p.d_err)) {
+                ok = false;
+                break;
+            }
+            for (int x = 0; x < 2; ++x) {
+                if (j >= nt[x]) continue;
+                // P_X(j) published by its softmax (which read S_X(j) first)
+                if (!pv(x, j)) { ok = false; break; }
+                if (j + 1 < nt[x]) {
+                    if (!k_next) {
+                        if (!pf_wait_warp(&bars->k_full[(j + 1) % kKStages],
+                                          ((j + 1) / kKStages) & 1, bars, p.d_err)) {
+                            ok = false;
+                            break;
                         }
-                        qk(x, j + 1);  // overwrites P_X(j) after the P*V above consumed it
+                        tc::fence_after_sync();
+                        k_next = true;
                     }
+                    qk(x, j + 1);  // overwrites P_X(j) after the P*V above consumed it
                 }
-                if (!ok) break;
-                tc::commit(&bars->v_empty[j % kVStages]);
-                if (more) {
-                    if (!k_next) {  // neither q-tile uses K_{j+1}: still release its stage
-                        if (!pf_wait(&bars->k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1,
-                                     bars, p.d_err)) { ok = false; break; }
-                    }
-                    tc::commit(&bars->k_empty[(j + 1) % kKStages]);
+            }
+            if (!ok) break;
+            tc::commit_warp(&bars->v_empty[j % kVStages]);
+            if (more) {
+                if (!k_next) {  // neither q-tile uses K_{j+1}: still release its stage
+                    if (!pf_wait_warp(&bars->k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1,
+                                      bars, p.d_err)) { ok = false; break; }
                 }
+                tc::commit_warp(&bars->k_empty[(j + 1) % kKStages]);
             }
         }
         __syncwarp();
@@ -558,17 +535,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             }
             // P = 2^(s*scale - m) as fp16 pairs over the S columns already read;
             // each half of 64 keys is published as soon as it is stored
-            const float neg_m = -m_used;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
+            const float2 sc2 = make_float2(sc, sc), negm2 = make_float2(-m_used, -m_used);
+            float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // partial row sums
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sr[c][e]), sc, neg_m));
-                    const float p1 = ex2(fmaf(__uint_as_float(sr[c][e + 1]), sc, neg_m));
-                    ls[(e >> 1) & 3] += p0 + p1;
-                    pk[e >> 1] = pack_f16(p0, p1);
+                    const float2 xx = __ffma2_rn(
+                        make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sc2,
+                        negm2);
+                    const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
+                    ls[(e >> 1) & 1] = __fadd2_rn(ls[(e >> 1) & 1], pp);
+                    pk[e >> 1] = pack_f16(pp.x, pp.y);
                 }
                 tmem_st16(sX + c * 16, pk);
                 if (c & 1) {
@@ -577,7 +556,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     mbar_arrive(&bars->p_full[x][c >> 1]);
                 }
             }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            l += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
         }
         // epilogue: O / l -> out
         if (ok && nt_x > 0) ok = pf_wait_warp(&bars->o_done[x], (nt_x - 1) & 1, bars, p.d_err);

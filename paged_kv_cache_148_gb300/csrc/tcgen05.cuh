@@ -86,6 +86,41 @@ PA_DEVICE void commit(uint64_t* bar) {
         ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Warp-collective issue: every lane of a converged warp makes the call and
+// elect.sync picks the lane that issues the instruction (the same lane each
+// time, so the in-order and commit rules for one issuing thread hold).  With
+// the warp converged its operands stay in warp-uniform registers, which keeps
+// the issue cost per MMA low while other warps on the same scheduler are busy.
+PA_DEVICE void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// The same with A read from TMEM.
+PA_DEVICE void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// commit() by the elected lane of a converged warp.
+PA_DEVICE void commit_warp(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+        ::"r"(smem_u32(bar)) : "memory");
+}
+
 // ----------------------------------------------------------------- TMEM <-> registers
 // 32 lanes x 32 columns of 32-bit: thread t of the warp gets lane (quarter*32 + t).
 PA_DEVICE void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
