@@ -256,10 +256,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks;
-        auto load_rows = [&](int j) -> int32_t {  // this lane's page of tile j
+        // this lane's page of tile j: the table read is issued one tile ahead
+        // (fetch_id) and checked only when the tile is loaded (tile_row), so the
+        // warp never stalls on it
+        auto lane_page = [&](int j) {
             const int e = j * pages_per_tile + lane;
-            if (lane >= pages_per_tile || (e << p.log2_bp) >= kv_end) return -1;
-            int32_t id = e < p.max_blocks ? __ldg(table + e) : -1;
+            return (lane < pages_per_tile && (e << p.log2_bp) < kv_end) ? e : -1;
+        };
+        auto fetch_id = [&](int j) -> int32_t {
+            const int e = lane_page(j);
+            return (e >= 0 && e < p.max_blocks) ? __ldg(table + e) : -1;
+        };
+        auto tile_row = [&](int j, int32_t id) -> int32_t {
+            if (lane_page(j) < 0) return -1;
             if (id < 0 || id >= p.num_blocks) {
                 set_error(p.d_err, id < 0 ? PA_ERR_NEGATIVE_BLOCK : PA_ERR_OUT_OF_RANGE);
                 id = 0;  // stay in bounds; the result is flagged as invalid
@@ -284,7 +293,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                                 q_begin + q0 + QT, &bars->q_full);
             }
         }
-        int32_t next_row = load_rows(0);  // prefetched ids of tile kn
+        int32_t next_id = fetch_id(0);  // prefetched table entry of tile kn
         int kn = 0, vn = 0;
         uint64_t t_idle = 0;
         uint32_t spins = 0;
@@ -293,11 +302,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             int go = 0;
             if (lane == 0)
                 go = kn < n_tiles && kn < vn + kIdRing &&  // page ids of tiles vn..kn stay live
-                     (kn < kKStages || mbar_try_wait(&bars->k_empty[kn % kKStages],
+                     (kn < kKStages || mbar_test_wait(&bars->k_empty[kn % kKStages],
                                                      ((kn / kKStages) - 1) & 1));
             if (__shfl_sync(0xffffffffu, go, 0)) {
-                const int row = next_row;
-                if (kn + 1 < n_tiles) next_row = load_rows(kn + 1);
+                const int row = tile_row(kn, next_id);
+                if (kn + 1 < n_tiles) next_id = fetch_id(kn + 1);
                 bars->page_row[kn % kIdRing][lane] = row;
                 const int loaded = loaded_pages(kn);
                 uint64_t* bar = &bars->k_full[kn % kKStages];
@@ -314,7 +323,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             go = 0;
             if (lane == 0)
                 go = vn < n_tiles && vn < kn &&
-                     (vn < kVStages || mbar_try_wait(&bars->v_empty[vn % kVStages],
+                     (vn < kVStages || mbar_test_wait(&bars->v_empty[vn % kVStages],
                                                      ((vn / kVStages) - 1) & 1));
             if (__shfl_sync(0xffffffffu, go, 0)) {
                 const int row = bars->page_row[vn % kIdRing][lane];
@@ -446,13 +455,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 const uint32_t vrow = vbase + r * 128;
                 if (j * kPfKeys + r < zlim) {
                     // chunk order rotated by the row: 8 threads of a 128-bit phase hit
-                    // 8 different bank groups
+                    // 8 different bank groups.  Eight loads go out before the first
+                    // store so their latencies overlap.
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const uint32_t a = vrow + (c >> 3) * kHalf + ((c + r) & 7) * 16;
-                        const uint4 x = ld_shared_v4(a);
-                        st_shared_v4(a, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y),
-                                     bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
+                    for (int hb = 0; hb < 2; ++hb) {
+                        uint4 x[8];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            x[c] = ld_shared_v4(vrow + hb * kHalf + ((c + r) & 7) * 16);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            st_shared_v4(vrow + hb * kHalf + ((c + r) & 7) * 16,
+                                         bf16x2_to_f16x2(x[c].x), bf16x2_to_f16x2(x[c].y),
+                                         bf16x2_to_f16x2(x[c].z), bf16x2_to_f16x2(x[c].w));
                     }
                 } else {
 #pragma unroll
