@@ -77,18 +77,6 @@ PA_DEVICE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking probe of phase `parity` (try_wait may suspend the thread for a
-// while; a loop that polls several barriers wants an immediate answer).
-PA_DEVICE bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
-    return ok != 0;
-}
-
 // Wait for phase `parity` of `bar` to complete, for at most ~timeout_ns.
 // Returns false (and records PA_ERR_TIMEOUT) if the wait ran out.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legal wait

@@ -84,10 +84,7 @@ struct PrefillParams {
     int32_t* d_err;
 };
 
-constexpr int kIdRing = 4;  // tiles of page ids kept for the V loads
-
 struct PfBars {
-    int32_t page_row[kIdRing][32];  // pool row of each page of a tile (128 / B_p <= 16 used)
     uint64_t q_full;
     uint64_t k_full[kKStages];
     uint64_t k_empty[kKStages];
@@ -293,69 +290,38 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                                 q_begin + q0 + QT, &bars->q_full);
             }
         }
-        int32_t next_id = fetch_id(0);  // prefetched table entry of tile kn
-        int kn = 0, vn = 0;
-        uint64_t t_idle = 0;
-        uint32_t spins = 0;
-        while (kn < n_tiles || vn < n_tiles) {
-            bool moved = false;
-            int go = 0;
-            if (lane == 0)
-                go = kn < n_tiles && kn < vn + kIdRing &&  // page ids of tiles vn..kn stay live
-                     (kn < kKStages || mbar_test_wait(&bars->k_empty[kn % kKStages],
-                                                     ((kn / kKStages) - 1) & 1));
-            if (__shfl_sync(0xffffffffu, go, 0)) {
-                const int row = tile_row(kn, next_id);
-                if (kn + 1 < n_tiles) next_id = fetch_id(kn + 1);
-                bars->page_row[kn % kIdRing][lane] = row;
-                const int loaded = loaded_pages(kn);
-                uint64_t* bar = &bars->k_full[kn % kKStages];
-                if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)loaded * bp * 128 * 2);
-                __syncwarp();
-                if (lane < loaded) {
-                    unsigned char* dst = smem + kOffK + (kn % kKStages) * kTile + lane * bp * 128;
-                    tc::tma_load_2d(dst, &tmap_k, 0, row, bar);
-                    tc::tma_load_2d(dst + kHalf, &tmap_k, 64, row, bar);
-                }
-                ++kn;
-                moved = true;
+        // K_j then V_j for every tile, each as soon as its stage is released: K_j
+        // once Q K_{j-2}^T has completed, V_j once P V_{j-3} has.  Both releases
+        // come from the same MMA commit point, so blocking on them in this order
+        // never holds back a load that could already go.
+        int32_t next_id = fetch_id(0);  // prefetched table entry of tile j
+        for (int j = 0; j < n_tiles; ++j) {
+            if (j >= kKStages &&
+                !pf_wait_warp(&bars->k_empty[j % kKStages], ((j / kKStages) - 1) & 1, bars, p.d_err))
+                break;
+            const int row = tile_row(j, next_id);
+            if (j + 1 < n_tiles) next_id = fetch_id(j + 1);
+            const int loaded = loaded_pages(j);
+            const uint32_t bytes = (uint32_t)loaded * bp * 128 * 2;
+            uint64_t* kbar = &bars->k_full[j % kKStages];
+            if (lane == 0) mbar_arrive_expect_tx(kbar, bytes);
+            __syncwarp();
+            if (lane < loaded) {
+                unsigned char* dst = smem + kOffK + (j % kKStages) * kTile + lane * bp * 128;
+                tc::tma_load_2d(dst, &tmap_k, 0, row, kbar);
+                tc::tma_load_2d(dst + kHalf, &tmap_k, 64, row, kbar);
             }
-            go = 0;
-            if (lane == 0)
-                go = vn < n_tiles && vn < kn &&
-                     (vn < kVStages || mbar_test_wait(&bars->v_empty[vn % kVStages],
-                                                     ((vn / kVStages) - 1) & 1));
-            if (__shfl_sync(0xffffffffu, go, 0)) {
-                const int row = bars->page_row[vn % kIdRing][lane];
-                const int loaded = loaded_pages(vn);
-                uint64_t* bar = &bars->v_full[vn % kVStages];
-                if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)loaded * bp * 128 * 2);
-                __syncwarp();
-                if (lane < loaded) {
-                    unsigned char* dst = smem + kOffV + (vn % kVStages) * kTile + lane * bp * 128;
-                    tc::tma_load_2d(dst, &tmap_v, 0, row, bar);
-                    tc::tma_load_2d(dst + kHalf, &tmap_v, 64, row, bar);
-                }
-                ++vn;
-                moved = true;
+            if (j >= kVStages &&
+                !pf_wait_warp(&bars->v_empty[j % kVStages], ((j / kVStages) - 1) & 1, bars, p.d_err))
+                break;
+            uint64_t* vbar = &bars->v_full[j % kVStages];
+            if (lane == 0) mbar_arrive_expect_tx(vbar, bytes);
+            __syncwarp();
+            if (lane < loaded) {
+                unsigned char* dst = smem + kOffV + (j % kVStages) * kTile + lane * bp * 128;
+                tc::tma_load_2d(dst, &tmap_v, 0, row, vbar);
+                tc::tma_load_2d(dst + kHalf, &tmap_v, 64, row, vbar);
             }
-            if (moved) {
-                t_idle = 0;
-                continue;
-            }
-            int stop = 0;
-            if (lane == 0 && (++spins & 255u) == 0) {
-                if (*(volatile int32_t*)&bars->abort) stop = 1;
-                const uint64_t now = global_timer_ns();
-                if (t_idle == 0) {
-                    t_idle = now;
-                } else if (now - t_idle > kWaitLimitNs) {
-                    set_error(p.d_err, PA_ERR_TIMEOUT);
-                    *(volatile int32_t*)&bars->abort = 1;
-                    stop = 1;
-                }
-            }
-            if (__shfl_sync(0xffffffffu, stop, 0)) break;
         }
         __syncwarp();
     } else if (warp == 1) {
