@@ -55,6 +55,10 @@ def parse():
     ap.add_argument("--l2", choices=["none", "flush"], default="none",
                     help="none: the step's K/V (4x the 129 MB L2) is itself larger than L2; "
                          "flush: write a 256 MiB buffer before every timed step")
+    ap.add_argument("--path", choices=["fused", "split"], default="split",
+                    help="decode step: split = pa_write_kv + pa_decode_partial + pa_decode_merge "
+                         "(dependent launches; fastest on large batches); fused = pa_decode_step "
+                         "(write + attention + merge in one launch; fastest on small batches)")
     ap.add_argument("--partition-tokens", type=int, default=0,
                     help="split-KV partition size for decode (0 = the library's choice)")
     return ap.parse_args()
@@ -158,6 +162,7 @@ class ClockSampler:
 # --------------------------------------------------------------------------- traffic record
 KERNEL_SOURCES = {
     "decode_partition_kernel": ("decode.cu", "common.cuh"),
+    "decode_step": ("decode.cu", "common.cuh"),
     "prefill_kernel": ("prefill.cu", "tcgen05.cuh", "common.cuh"),
 }
 
@@ -298,10 +303,14 @@ def run_ours(args, rank, world, local_rank):
         g.set_partition_tokens(args.partition_tokens)
     stream = torch.cuda.current_stream(dev)
     is_decode = wl.kind == "decode"
+    fused = is_decode and args.path == "fused"
     max_parts = g.max_parts()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step():
+        if fused:
+            g.step(stream, fused=True)
+            return
         g.write_new(stream)
         if is_decode:
             g.attend(stream, "partial")
@@ -346,6 +355,12 @@ def run_ours(args, rank, world, local_rank):
             flush.fill_(i & 255)
         e = evk[i]
         e[0].record(stream)
+        if fused:  # one kernel: write + attention + merge
+            e[1].record(stream)
+            g.step(stream, fused=True)
+            e[2].record(stream)
+            e[3].record(stream)
+            continue
         g.write_new(stream)
         e[1].record(stream)
         if is_decode:
@@ -366,7 +381,7 @@ def run_ours(args, rank, world, local_rank):
     ms = max_over_ranks(float(step_ms.mean()), world, dev)
 
     # end-to-end through the public API with host buffers
-    e2e = run_e2e(args, g, stream, dev, is_decode)
+    e2e = run_e2e(args, g, stream, dev, is_decode, fused)
 
     hbm_peak, tf_peak, peak_src = measured_peaks()
     ab = algorithmic_bytes(wl)
@@ -385,6 +400,10 @@ def run_ours(args, rank, world, local_rank):
                   "no flush: inputs larger than L2 (the step reads %.0f MB of K/V, L2 is 129 MB)"
                   % (ab_kv_mb(wl))),
            "split_kv_partitions_max": max_parts,
+           "path": ("fused: pa_decode_step (new-token write, attention and split-KV merge in one "
+                    "launch)" if fused else
+                    "split: pa_write_kv + pa_decode_partial + pa_decode_merge" if is_decode else
+                    "pa_write_kv + pa_prefill"),
            "partition_tokens": args.partition_tokens or "auto"}
     if is_decode:
         per_rank = ab["decode_total"]
@@ -395,14 +414,20 @@ def run_ours(args, rank, world, local_rank):
                     "pct_of_nominal_8tbs": 100.0 * (per_rank / (ms * 1e-3) / 1e9) / 8000.0})
         part_ms = float(attn_ms.mean())
         achieved = per_rank / (part_ms * 1e-3) / 1e9
-        res["roofline"] = {"kernel": "decode_partition_kernel", "bound": "hbm",
+        kname = "decode_step" if fused else "decode_partition_kernel"
+        res["roofline"] = {"kernel": ("decode_partition_kernel (fused step)" if fused else kname),
+                           "bound": "hbm",
                            "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                            "frac": achieved / hbm_peak, "peak_source": peak_src + " hbm_gbs",
-                           "traffic": recorded_traffic("decode_partition_kernel", wl.name),
+                           "traffic": recorded_traffic(kname, wl.name),
                            "algorithmic_bytes": per_rank, "launch_ms": part_ms}
-        res["kernel_ms"] = {"write_kv": float(write_ms.mean()),
-                            "decode_partition": part_ms, "decode_merge": float(merge_ms.mean())}
-        launches = K * (2 + (1 if max_parts > 1 else 0))
+        if fused:
+            res["kernel_ms"] = {"decode_step": part_ms}
+            launches = K
+        else:
+            res["kernel_ms"] = {"write_kv": float(write_ms.mean()), "decode_partition": part_ms,
+                                "decode_merge": float(merge_ms.mean())}
+            launches = K * (2 + (1 if max_parts > 1 else 0))
     else:
         flops = prefill_flops(wl)
         res.update({"metric": "paged chunked-prefill TFLOP/s (causal-visible) on 1 GB300",
@@ -427,7 +452,7 @@ def run_ours(args, rank, world, local_rank):
     return res, wl, ab
 
 
-def run_e2e(args, g, stream, dev, is_decode):
+def run_e2e(args, g, stream, dev, is_decode, fused=False):
     """Same step through the public API with pinned host buffers, copies timed."""
     import torch
     wl = g.wl
@@ -449,7 +474,7 @@ def run_e2e(args, g, stream, dev, is_decode):
     def one():
         for k, t in pinned.items():
             dev_bufs[k].copy_(t, non_blocking=True)
-        g.step(stream)
+        g.step(stream, fused=fused)
         out_host.copy_(g.out, non_blocking=True)
 
     for i in range(3):

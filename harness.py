@@ -12,7 +12,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from paged_kv_cache_148_gb300 import decode, decode_workspace_bytes, prefill, write_kv
+from paged_kv_cache_148_gb300 import (decode, decode_step, decode_step_workspace,
+                                      decode_workspace_bytes, prefill, write_kv)
 from paged_kv_cache_148_gb300.cache import PagedCache
 
 WRITE_CHUNK = 32768  # tokens per host->device batch while filling the cache
@@ -95,11 +96,15 @@ class GpuWorkload:
 
     def _alloc_workspace(self):
         if self.wl.kind != "decode":
-            self.workspace = None
+            self.workspace = self.step_workspace = None
             return
         nb = decode_workspace_bytes(self.cache.pool, self.wl.num_seqs, self.wl.num_q_heads,
                                     self.max_context, self.partition_tokens)
         self.workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=self.device)
+        # pa_decode_step: zero-filled once, its semaphores return to zero every call
+        self.step_workspace = decode_step_workspace(self.cache.pool, self.wl.num_seqs,
+                                                    self.wl.num_q_heads, self.max_context,
+                                                    self.partition_tokens)
 
     def set_partition_tokens(self, n: int):
         self.partition_tokens = int(n)
@@ -120,8 +125,19 @@ class GpuWorkload:
                        self.block_tables, self.max_q, self.max_context, wl.scale,
                        causal=wl.causal, out=self.out, d_err=self.err, stream=stream)
 
-    def step(self, stream=None):
-        """One pass of the hot path: scatter this step's K/V, then attention."""
+    def attend_fused(self, stream=None):
+        """Decode only: this step's new token written and attended in one launch."""
+        wl = self.wl
+        return decode_step(self.cache.pool, self.k_new, self.v_new, self.slot_mapping, self.q,
+                           self.block_tables, self.context_lens, self.max_context, wl.scale,
+                           self.step_workspace, out=self.out,
+                           partition_tokens=self.partition_tokens, d_err=self.err, stream=stream)
+
+    def step(self, stream=None, fused: bool = False):
+        """One pass of the hot path: scatter this step's K/V, then attention
+        (for decode with fused=True: both in pa_decode_step's single launch)."""
+        if fused and self.wl.kind == "decode":
+            return self.attend_fused(stream)
         self.write_new(stream)
         return self.attend(stream)
 

@@ -232,6 +232,44 @@ pa_status pa_decode_noalloc(const pa_kv_pool* pool, const void* q, int32_t num_q
                             pa_stream_t stream);
 
 /*
+ * One decode step in a single launch: the fused form of pa_write_kv of one
+ * new token per sequence followed by pa_decode (P1 §4.1: the new K/V go to
+ * their slots, then attention reads them through the table; P1 §4: split-KV
+ * partitions and the merge of their softmax states).  For every (sequence s,
+ * kv-head h) the partition that holds position n - 1 (n = context_lens[s])
+ * first writes k_new[s][h] and v_new[s][h] into slot slot_mapping[s], then
+ * all partitions attend exactly as in pa_decode, and the last partition of
+ * (s, h) to finish merges the group's partials into `out`.
+ *   k_new, v_new:  device [num_seqs][num_kv_heads][head_dim], pool dtype,
+ *                  16-byte aligned.
+ *   slot_mapping:  device int64 [num_seqs]: the slot of position n - 1 under
+ *                  block_tables[s] (any copy-on-write of that block must be
+ *                  enqueued before).  Another slot inside the pool sets
+ *                  *d_err = PA_ERR_INVALID_ARG, one outside it
+ *                  PA_ERR_OUT_OF_RANGE; the row is then not written.
+ *   workspace:     >= pa_decode_step_workspace_bytes(...) bytes, 16-byte
+ *                  aligned (may be NULL when that size is 0), and ZERO-FILLED
+ *                  before its first use (one cudaMemsetAsync after
+ *                  allocation).  It holds the partials and one int32
+ *                  semaphore per (sequence, kv-head); every call returns the
+ *                  semaphores to zero, so the same workspace serves all later
+ *                  calls of the same shape, including replays of a captured
+ *                  CUDA graph.  Calls that share a workspace must be ordered
+ *                  on one stream.
+ * Other arguments, limits and errors as pa_decode.  Allocates nothing and
+ * enqueues one kernel.
+ */
+pa_status pa_decode_step_workspace_bytes(const pa_kv_pool* pool, int32_t num_seqs,
+                                         int32_t num_q_heads, int32_t max_context,
+                                         int32_t partition_tokens, size_t* bytes);
+pa_status pa_decode_step(const pa_kv_pool* pool, const void* k_new, const void* v_new,
+                         const int64_t* slot_mapping, const void* q, int32_t num_q_heads,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                         const int32_t* context_lens, int32_t num_seqs, int32_t max_context,
+                         float scale, int32_t partition_tokens, float* out, void* workspace,
+                         size_t workspace_bytes, int32_t* d_err, pa_stream_t stream);
+
+/*
  * Paged chunked-prefill attention on tensor cores (P1 §4: prefill reuses a
  * flash-style tiled kernel fed the paged table; paging and IO-aware tiling
  * are orthogonal).  Sequence s has new query tokens

@@ -40,7 +40,8 @@ EXPORTED = [
     "pa_status_str", "pa_last_cuda_error", "pa_abi_version", "pa_page_size_bytes",
     "pa_physical_slot", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks",
     "pa_decode_partition_tokens", "pa_decode_workspace_bytes", "pa_decode", "pa_decode_partial",
-    "pa_decode_merge", "pa_decode_noalloc", "pa_prefill",
+    "pa_decode_merge", "pa_decode_noalloc", "pa_decode_step_workspace_bytes", "pa_decode_step",
+    "pa_prefill",
     "pa_alloc_create", "pa_alloc_destroy", "pa_alloc_append", "pa_alloc_fork",
     "pa_alloc_writable_tail", "pa_alloc_reserve", "pa_alloc_release", "pa_alloc_refcount",
     "pa_alloc_num_free",
@@ -95,6 +96,8 @@ def lib() -> ctypes.CDLL:
         "pa_decode_partial": ([P, P, i32, P, i32, P, i32, i32, f32, i32, P, P, sz, P, P], i32),
         "pa_decode_merge": ([P, i32, P, i32, i32, i32, P, P, sz, P], i32),
         "pa_decode_noalloc": ([P, P, i32, P, i32, P, i32, i32, f32, i32, P, P, P], i32),
+        "pa_decode_step_workspace_bytes": ([P, i32, i32, i32, i32, P], i32),
+        "pa_decode_step": ([P, P, P, P, P, i32, P, i32, P, i32, i32, f32, i32, P, P, sz, P, P], i32),
         "pa_prefill": ([P, P, i32, i32, P, P, P, i32, i32, i32, i32, f32, i32, P, P, P], i32),
         "pa_alloc_create": ([i32, P, P], i32),
         "pa_alloc_destroy": ([P], None),
@@ -277,6 +280,54 @@ def decode(pool: KVPool, q: torch.Tensor, block_tables: torch.Tensor, context_le
               _ptr(context_lens), B, int(max_context), float(scale), int(partition_tokens),
               _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_err), _stream(stream)),
            "pa_decode" if phase == "all" else "pa_decode_partial")
+    return out
+
+
+def decode_step_workspace_bytes(pool: KVPool, num_seqs: int, num_q_heads: int, max_context: int,
+                                partition_tokens: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().pa_decode_step_workspace_bytes(pool.c, num_seqs, num_q_heads, max_context,
+                                                partition_tokens, ctypes.byref(out)),
+           "pa_decode_step_workspace_bytes")
+    return out.value
+
+
+def decode_step_workspace(pool: KVPool, num_seqs: int, num_q_heads: int, max_context: int,
+                          partition_tokens: int = 0) -> Optional[torch.Tensor]:
+    """A zero-filled workspace for decode_step (reusable for every later call of the shape)."""
+    n = decode_step_workspace_bytes(pool, num_seqs, num_q_heads, max_context, partition_tokens)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=pool.device) if n > 0 else None
+
+
+def decode_step(pool: KVPool, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                q: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                max_context: int, scale: float, workspace: Optional[torch.Tensor],
+                out: Optional[torch.Tensor] = None, partition_tokens: int = 0,
+                d_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """pa_decode_step: write each sequence's new token and attend, in one launch.
+
+    workspace comes from decode_step_workspace() (zero-filled once, then reused).
+    """
+    _need(k_new, "k_new", pool.dtype, pool.device)
+    _need(v_new, "v_new", pool.dtype, pool.device)
+    _need(slot_mapping, "slot_mapping", torch.int64, pool.device)
+    _need(q, "q", pool.dtype, pool.device)
+    _need(block_tables, "block_tables", torch.int32, pool.device)
+    _need(context_lens, "context_lens", torch.int32, pool.device)
+    B, Hq, D = q.shape
+    if tuple(k_new.shape) != (B, pool.num_kv_heads, pool.head_dim) or k_new.shape != v_new.shape:
+        raise ValueError("k_new/v_new must be [B][H_kv][D]")
+    if tuple(slot_mapping.shape) != (B,):
+        raise ValueError("slot_mapping must be [B]")
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=pool.device)
+    _need(out, "out", torch.float32, pool.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode_step(pool.c, _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(q), Hq,
+                                _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+                                B, int(max_context), float(scale), int(partition_tokens), _ptr(out),
+                                _ptr(workspace), ws_bytes, _ptr(d_err), _stream(stream)),
+           "pa_decode_step")
     return out
 
 

@@ -31,6 +31,12 @@
 //  * The CTA's warps combine in shared memory; a single-partition sequence
 //    writes the normalised output directly, otherwise (m, l, acc) partials go
 //    to the workspace and decode_merge_kernel finishes.
+//  * Fused step (pa_decode_step): the same kernel also writes the new token
+//    of (sequence, kv-head) into its slot, and into the shared-memory copy of
+//    the chunk that holds it (P1 §4.1), and the last partition CTA of each
+//    (sequence, kv-head) to finish -- counted by a semaphore in the
+//    workspace -- merges the group's partials, so a decode step is one
+//    launch.
 #include <cfloat>
 #include <cmath>
 
@@ -64,6 +70,11 @@ struct DecodeParams {
     float* ws_l;
     float* ws_acc;
     int32_t* d_err;
+    // fused step only
+    const unsigned char* k_new;   // [B][H_kv][D] new rows
+    const unsigned char* v_new;
+    const int64_t* slot_mapping;  // [B] slot of position context_lens[s] - 1
+    int32_t* sem;                 // [B][H_kv] partitions finished (zero between calls)
 };
 
 template <typename T>
@@ -176,7 +187,102 @@ PA_DEVICE void issue_chunk(const DecodeParams& p, int s, int h, int n, int c, in
     }
 }
 
-template <typename T, int G, int W, int S>
+// atomicAdd with release-acquire semantics at GPU scope
+PA_DEVICE int atom_add_acq_rel_gpu(int32_t* p, int v) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Fused step: merge of the (m, l, acc) partials of the G heads of (s, h),
+// run by the last partition CTA of the group (same math as
+// decode_merge_kernel).  `sm` is free shared memory (the ring).
+template <int G, int D, int W>
+PA_DEVICE void merge_group(const DecodeParams& p, int s, int h, int n_parts, float* sm) {
+    constexpr int kCap = 1024;                // partitions per pass through shared memory
+    constexpr int NV = G * D / 4;             // float4 outputs of the group
+    constexpr int NO = (NV + W * 32 - 1) / (W * 32);
+    constexpr int U = 4;                      // partitions per batch of independent loads
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t qh0 = (int64_t)s * p.num_q_heads + (int64_t)h * G;
+    float* Mh = sm;
+    float* Lh = sm + G;
+    float* wts = sm + 2 * G;
+    // maxima over the partitions, one warp per head
+    for (int g = warp; g < G; g += W) {
+        const float* mrow = p.ws_m + (qh0 + g) * p.max_parts;
+        float M = -INFINITY;
+        for (int i = lane; i < n_parts; i += 32) M = fmaxf(M, __ldcg(mrow + i));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+        if (lane == 0) {
+            Mh[g] = M;
+            Lh[g] = 0.f;
+        }
+    }
+    float4 a[NO];
+#pragma unroll
+    for (int k = 0; k < NO; ++k) a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = 0; p0 < n_parts; p0 += kCap) {
+        const int cnt = min(kCap, n_parts - p0);
+        __syncthreads();  // maxima ready / previous weights consumed
+        for (int g = warp; g < G; g += W) {
+            const int64_t r0 = (qh0 + g) * p.max_parts + p0;
+            float ls = 0.f;
+            for (int i = lane; i < cnt; i += 32) {
+                const float w = ex2(__ldcg(p.ws_m + r0 + i) - Mh[g]);
+                wts[g * kCap + i] = w;
+                ls = fmaf(__ldcg(p.ws_l + r0 + i), w, ls);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(kFull, ls, off);
+            if (lane == 0) Lh[g] += ls;
+        }
+        __syncthreads();
+        // every thread's outputs advance together over U partitions at a time,
+        // so U * NO independent 16-byte loads are in flight
+        for (int i0 = 0; i0 < cnt; i0 += U) {
+            float4 v[NO][U];
+#pragma unroll
+            for (int k = 0; k < NO; ++k) {
+                const int idx = threadIdx.x + k * W * 32;
+                const int g = idx / (D / 4), d4 = idx - g * (D / 4);
+                const float4* ar = reinterpret_cast<const float4*>(
+                    p.ws_acc + ((qh0 + g) * p.max_parts + p0) * D) + d4;
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    v[k][u] = (idx < NV && i0 + u < cnt) ? __ldcg(ar + (int64_t)(i0 + u) * (D / 4))
+                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < NO; ++k) {
+                const int idx = threadIdx.x + k * W * 32;
+                const int g = min(idx / (D / 4), G - 1);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const float w = i0 + u < cnt ? wts[g * kCap + i0 + u] : 0.f;
+                    a[k].x = fmaf(v[k][u].x, w, a[k].x);
+                    a[k].y = fmaf(v[k][u].y, w, a[k].y);
+                    a[k].z = fmaf(v[k][u].z, w, a[k].z);
+                    a[k].w = fmaf(v[k][u].w, w, a[k].w);
+                }
+            }
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < NO; ++k) {
+        const int idx = threadIdx.x + k * W * 32;
+        if (idx < NV) {
+            const int g = idx / (D / 4), d4 = idx - g * (D / 4);
+            const float inv = 1.f / Lh[g];
+            reinterpret_cast<float4*>(p.out + (qh0 + g) * D)[d4] =
+                make_float4(a[k].x * inv, a[k].y * inv, a[k].z * inv, a[k].w * inv);
+        }
+    }
+}
+
+template <typename T, int G, int W, int S, bool kFused>
 __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodeParams p) {
     using R = Row<T>;
     constexpr int EPL = R::N;                 // elements of a row per lane
@@ -241,12 +347,37 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
                        &masks[stage]);
     };
 
+    // fused step: the warp that streams the chunk holding position n - 1 loads
+    // the new token's row of (s, h) now (K in lanes 0-15, V in lanes 16-31,
+    // 16 bytes each) and, once that chunk is in shared memory, stores it both
+    // to its slot in the pool and over the chunk's copy of the row -- the bulk
+    // copy may have read the slot before or after the store, the attention
+    // uses the new row either way
+    const int last_chunk = n_chunks - 1;
+    const bool owner = kFused && c_end == n_chunks && last_chunk >= first &&
+                       (last_chunk - first) % W == 0;
+    // kept in shared memory so that no registers stay live through the main loop
+    __shared__ uint4 new_row[32];
+    __shared__ int64_t new_slot;
+    __shared__ int32_t last_pid;  // table entry of the page holding position n - 1
+    uint4 row_reg = make_uint4(0, 0, 0, 0);
+    if (owner) {
+        const int64_t src = ((int64_t)s * p.num_kv_heads + h) * kRowBytes + (lane & 15) * 16;
+        row_reg = __ldg(reinterpret_cast<const uint4*>((lane < 16 ? p.k_new : p.v_new) + src));
+        if (lane == 0) {
+            new_slot = __ldg(p.slot_mapping + s);
+            const int e = (n - 1) >> p.log2_bp;
+            last_pid = e < p.max_blocks ? __ldg(table + e) : -1;
+        }
+    }
+
     // prologue: first S chunks in flight
 #pragma unroll
     for (int i = 0; i < S; ++i) {
         const int32_t id = __shfl_sync(kFull, id_reg, i & 31);
         if (lane == 0 && i < my_n) issue(i, id);
     }
+    if (owner) new_row[lane] = row_reg;  // the loads completed behind the prologue's copies
 
     // per-lane constants of the transpose-reduce layout
     const int half = lane >> 4;               // which row of a row pair
@@ -299,6 +430,29 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
         const bool masked = vmask != 0xffffu;
         const unsigned char* kst = ring + (size_t)stage * 2 * kChunkBytes;
         const unsigned char* vst = kst + kChunkBytes;
+        if (owner && first + i * W == last_chunk) {
+            const int pos = n - 1;
+            const int64_t bpm = (1 << p.log2_bp) - 1;
+            const int64_t slot = new_slot;
+            const int32_t pid = last_pid;
+            int err = 0;
+            if (slot < 0 || slot >= ((int64_t)p.num_blocks << p.log2_bp))
+                err = PA_ERR_OUT_OF_RANGE;
+            else if (pid < 0 || (slot >> p.log2_bp) != pid || (slot & bpm) != (pos & bpm))
+                err = PA_ERR_INVALID_ARG;  // not the slot of the last position
+            if (err != 0) {
+                if (lane == 0) set_error(p.d_err, err);
+            } else {
+                const uint4 v = new_row[lane];
+                const int64_t row = ((int64_t)pid * p.num_kv_heads + h) * (bpm + 1) + (pos & bpm);
+                unsigned char* pool = const_cast<unsigned char*>(lane < 16 ? p.k_pool : p.v_pool);
+                *reinterpret_cast<uint4*>(pool + row * kRowBytes + (lane & 15) * 16) = v;
+                unsigned char* st = const_cast<unsigned char*>(lane < 16 ? kst : vst);
+                *reinterpret_cast<uint4*>(st + (pos & (kChunk - 1)) * kRowBytes + (lane & 15) * 16) = v;
+                fence_proxy_async_smem();  // before a later bulk copy refills this stage
+            }
+            __syncwarp();
+        }
 
         // ---- scores: partial dots over this lane's column, then transpose-reduce
         float part[NS];
@@ -448,7 +602,21 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
 
     // ---- combine the CTA's warps (reusing the ring) and write
     __syncthreads();
-    if (aborted) return;
+    if (aborted) {
+        if constexpr (!kFused) return;
+        // a fused step still counts this partition, so the group's semaphore
+        // returns to zero (the merged result is flagged invalid by *d_err)
+        if (n_parts > 1) {
+            __shared__ int last_aborted;
+            if (threadIdx.x == 0) {
+                const int old = atom_add_acq_rel_gpu(p.sem + (int64_t)s * p.num_kv_heads + h, 1);
+                last_aborted = old == n_parts - 1;
+                if (last_aborted) atomicExch(p.sem + (int64_t)s * p.num_kv_heads + h, 0);
+            }
+            __syncthreads();
+        }
+        return;
+    }
     // per warp: acc [G][D], then m [G], l [G]; the stride keeps float4 alignment
     float* cw = reinterpret_cast<float*>(smem);
     constexpr int MOFF = G * D, LOFF = G * D + G;
@@ -492,6 +660,24 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
                 p.ws_m[wi] = M;
                 p.ws_l[wi] = Lsum;
             }
+        }
+    }
+    if constexpr (kFused) {
+        if (n_parts > 1) {
+            // publish this partition's partials and count it: the barrier orders
+            // the CTA's stores before thread 0's release-acquire add, which makes
+            // them visible to whichever CTA of the group counts last; that one
+            // merges (its acquire orders the reads of the others' partials)
+            __shared__ int is_last;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                int32_t* sem = p.sem + (int64_t)s * p.num_kv_heads + h;
+                const int old = atom_add_acq_rel_gpu(sem, 1);
+                is_last = old == n_parts - 1;
+                if (is_last) atomicExch(sem, 0);  // every partition of the group has counted
+            }
+            __syncthreads();
+            if (is_last) merge_group<G, D, W>(p, s, h, n_parts, cw);
         }
     }
 }
@@ -602,11 +788,11 @@ static pa_status make_plan(const pa_kv_pool* pool, int32_t B, int32_t Hq, int32_
     return PA_OK;
 }
 
-template <typename T, int G>
+template <typename T, int G, bool kFused>
 static pa_status launch_partial(const DecodeParams& prm, int32_t B, int32_t Hkv, int32_t max_parts,
                                 cudaStream_t stream) {
     using Lay = DecodeSmem<kWarps, kStages, G>;
-    auto kern = decode_partition_kernel<T, G, kWarps, kStages>;
+    auto kern = decode_partition_kernel<T, G, kWarps, kStages, kFused>;
     static bool attr_done[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -628,14 +814,14 @@ static pa_status launch_partial(const DecodeParams& prm, int32_t B, int32_t Hkv,
     return launch_status();
 }
 
-template <typename T>
+template <typename T, bool kFused>
 static pa_status dispatch_group(int G, const DecodeParams& prm, int32_t B, int32_t Hkv,
                                 int32_t max_parts, cudaStream_t st) {
     switch (G) {
-        case 1: return launch_partial<T, 1>(prm, B, Hkv, max_parts, st);
-        case 2: return launch_partial<T, 2>(prm, B, Hkv, max_parts, st);
-        case 4: return launch_partial<T, 4>(prm, B, Hkv, max_parts, st);
-        case 8: return launch_partial<T, 8>(prm, B, Hkv, max_parts, st);
+        case 1: return launch_partial<T, 1, kFused>(prm, B, Hkv, max_parts, st);
+        case 2: return launch_partial<T, 2, kFused>(prm, B, Hkv, max_parts, st);
+        case 4: return launch_partial<T, 4, kFused>(prm, B, Hkv, max_parts, st);
+        case 8: return launch_partial<T, 8, kFused>(prm, B, Hkv, max_parts, st);
         default: return PA_ERR_UNSUPPORTED;
     }
 }
@@ -725,8 +911,8 @@ extern "C" pa_status pa_decode_partial(const pa_kv_pool* pool, const void* q,
     prm.d_err = d_err;
     cudaStream_t cs = (cudaStream_t)stream;
     if (pool->dtype == PA_DTYPE_F32)
-        return dispatch_group<float>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
-    return dispatch_group<uint16_t>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
+        return dispatch_group<float, false>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
+    return dispatch_group<uint16_t, false>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
 }
 
 extern "C" pa_status pa_decode_merge(const pa_kv_pool* pool, int32_t num_q_heads,
@@ -773,4 +959,87 @@ extern "C" pa_status pa_decode(const pa_kv_pool* pool, const void* q, int32_t nu
     if (st != PA_OK) return st;
     return pa_decode_merge(pool, num_q_heads, context_lens, num_seqs, max_context,
                            partition_tokens, out, workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------- fused step
+// Workspace of pa_decode_step: pa_decode's partials, then one int32 semaphore
+// per (sequence, kv-head), 256-byte aligned.
+static size_t step_sem_offset(const Plan& plan) { return align256(plan.ws_bytes); }
+
+static size_t step_workspace_bytes(const Plan& plan, int32_t B, int32_t Hkv) {
+    if (plan.max_parts <= 1) return 0;
+    return step_sem_offset(plan) + (size_t)B * Hkv * 4;
+}
+
+extern "C" pa_status pa_decode_step_workspace_bytes(const pa_kv_pool* pool, int32_t num_seqs,
+                                                    int32_t num_q_heads, int32_t max_context,
+                                                    int32_t partition_tokens, size_t* bytes) {
+    pa_status st = check_pool(pool);
+    if (st != PA_OK) return st;
+    if (!bytes) return PA_ERR_INVALID_ARG;
+    Plan plan;
+    st = make_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan);
+    if (st != PA_OK) return st;
+    *bytes = step_workspace_bytes(plan, num_seqs, pool->num_kv_heads);
+    return PA_OK;
+}
+
+extern "C" pa_status pa_decode_step(const pa_kv_pool* pool, const void* k_new, const void* v_new,
+                                    const int64_t* slot_mapping, const void* q,
+                                    int32_t num_q_heads, const int32_t* block_tables,
+                                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                    int32_t num_seqs, int32_t max_context, float scale,
+                                    int32_t partition_tokens, float* out, void* workspace,
+                                    size_t workspace_bytes, int32_t* d_err, pa_stream_t stream) {
+    pa_status st = check_pool(pool);
+    if (st != PA_OK) return st;
+    if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq < 0 || max_context < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!q || !block_tables || !context_lens || !out || !k_new || !v_new || !slot_mapping)
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % pool->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return PA_ERR_INVALID_ARG;
+    const int G = num_q_heads / pool->num_kv_heads;
+    if ((int64_t)pool->head_dim * dtype_bytes(pool->dtype) != kRowBytes) return PA_ERR_UNSUPPORTED;
+    if (!is_pow2(pool->block_size)) return PA_ERR_UNSUPPORTED;
+    if (pool->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(pool->k_pool) || !aligned16(pool->v_pool) ||
+        !aligned16(k_new) || !aligned16(v_new))
+        return PA_ERR_INVALID_ARG;
+    Plan plan;
+    st = make_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan);
+    if (st != PA_OK) return st;
+    if (plan.max_parts > 65535) return PA_ERR_UNSUPPORTED;
+    const size_t need = step_workspace_bytes(plan, num_seqs, pool->num_kv_heads);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+        return PA_ERR_INVALID_ARG;
+
+    DecodeParams prm = {};
+    prm.k_pool = static_cast<const unsigned char*>(pool->k_pool);
+    prm.v_pool = static_cast<const unsigned char*>(pool->v_pool);
+    prm.num_blocks = pool->num_blocks;
+    prm.log2_bp = ilog2(pool->block_size);
+    prm.num_kv_heads = pool->num_kv_heads;
+    prm.q = q;
+    prm.num_q_heads = num_q_heads;
+    prm.block_tables = block_tables;
+    prm.max_blocks = max_blocks_per_seq;
+    prm.context_lens = context_lens;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.part_chunks = plan.part_chunks;
+    prm.max_parts = plan.max_parts;
+    prm.out = out;
+    bind_workspace(plan, workspace, &prm);
+    prm.d_err = d_err;
+    prm.k_new = static_cast<const unsigned char*>(k_new);
+    prm.v_new = static_cast<const unsigned char*>(v_new);
+    prm.slot_mapping = slot_mapping;
+    prm.sem = need > 0 ? reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) +
+                                                    step_sem_offset(plan))
+                       : nullptr;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (pool->dtype == PA_DTYPE_F32)
+        return dispatch_group<float, true>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
+    return dispatch_group<uint16_t, true>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
 }
