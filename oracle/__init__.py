@@ -55,6 +55,8 @@ def _load():
         lib.orc_physical_slot.argtypes = [P, i64, i64, i64, P]
         lib.orc_decode.argtypes = [P, P, ctypes.c_int, i32, i32, i32, i32, P, i32, P, i32, P, i32,
                                    f64, P, i32, P]
+        lib.orc_decode_window.argtypes = [P, P, ctypes.c_int, i32, i32, i32, i32, P, i32, P,
+                                          i32, P, i32, i32, f64, P, i32, P]
         lib.orc_decode_contiguous.argtypes = [P, P, ctypes.c_int, i32, i32, i32, P, i32, P, i32,
                                               f64, P]
         lib.orc_decode_split.argtypes = [P, P, ctypes.c_int, i32, i32, i32, i32, P, i32, P, i32,
@@ -269,6 +271,31 @@ def decode(kpool, vpool, q, tables, context_lens, scale, rows=None) -> np.ndarra
     rc = lib.orc_decode(_ptr(kpool), _ptr(vpool), _dtype_code(kpool), N, Bp, H, D, _ptr(q), Hq,
                         _ptr(tab), tab.shape[1], _ptr(lens), B, float(scale),
                         None if r_arr is None else _ptr(r_arr), n_rows, _ptr(out))
+    _check(rc)
+    return out
+
+
+def decode_window(kpool, vpool, q, tables, context_lens, scale, window, rows=None) -> np.ndarray:
+    """Sliding-window decode in float64 (see attention.c: orc_decode_window): the
+    query at position n - 1 attends to positions max(0, n - window) .. n - 1;
+    window <= 0 means the whole context."""
+    lib = _load()
+    N, H, Bp, D = kpool.shape
+    q = np.ascontiguousarray(q)
+    B, Hq, _ = q.shape
+    tab = _tables_array(tables)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    if rows is None:
+        out = np.zeros((B, Hq, D), np.float64)
+        r_arr, n_rows = None, 0
+    else:
+        r_arr = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 2)
+        n_rows = r_arr.shape[0]
+        out = np.zeros((n_rows, D), np.float64)
+    rc = lib.orc_decode_window(_ptr(kpool), _ptr(vpool), _dtype_code(kpool), N, Bp, H, D,
+                               _ptr(q), Hq, _ptr(tab), tab.shape[1], _ptr(lens), B, int(window),
+                               float(scale), None if r_arr is None else _ptr(r_arr), n_rows,
+                               _ptr(out))
     _check(rc)
     return out
 

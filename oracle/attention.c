@@ -302,3 +302,76 @@ int orc_prefill(const void* kpool, const void* vpool, int dtype, int32_t num_blo
     }
     return err;
 }
+
+/*
+ * Sliding-window decode ("03｜PagedAttention 与 KV Cache 内存系统" §1.1 and §7:
+ * a sliding-window layer only uses the tokens inside its window; the window of
+ * the token at position p is [p - w + 1, p]).  The query is the token at
+ * position n - 1 (n = context_lens[s]), so it attends to positions
+ * max(0, n - window) .. n - 1 through the block table; window <= 0 means no
+ * window (all n positions, as orc_decode).  Same arguments and layout as
+ * orc_decode plus `window`.
+ */
+int orc_decode_window(const void* kpool, const void* vpool, int dtype, int32_t num_blocks,
+                      int32_t Bp, int32_t Hkv, int32_t D, const void* q, int32_t Hq,
+                      const int32_t* tables, int32_t max_blocks, const int32_t* context_lens,
+                      int32_t B, int32_t window, double scale, const int32_t* rows,
+                      int32_t n_rows, double* out) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || Bp <= 0 || B < 0) return -1;
+    int32_t G = Hq / Hkv;
+    int64_t total = rows ? n_rows : (int64_t)B * Hq;
+    int64_t maxn = 0;
+    for (int32_t s = 0; s < B; ++s) if (context_lens[s] > maxn) maxn = context_lens[s];
+    int err = 0;
+#pragma omp parallel
+    {
+        double* x = (double*)malloc(sizeof(double) * (size_t)(maxn > 0 ? maxn : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < total; ++r) {
+            int32_t s = rows ? rows[2 * r] : (int32_t)(r / Hq);
+            int32_t g = rows ? rows[2 * r + 1] : (int32_t)(r % Hq);
+            int32_t h = g / G;
+            int64_t n = context_lens[s];
+            int64_t lo = (window > 0 && n > window) ? n - window : 0;
+            const int32_t* table = tables + (size_t)s * max_blocks;
+            size_t q_off = ((size_t)s * Hq + g) * D;
+            double* o = out + (size_t)r * D;
+            int rc = 0;
+            if (n <= 0) rc = -1;
+            /* scores of the visible positions lo .. n-1 */
+            for (int64_t i = lo; i < n && !rc; ++i) {
+                int64_t slot;
+                rc = orc_physical_slot(table, max_blocks, Bp, i, &slot);
+                if (rc) break;
+                int64_t blk = slot / Bp, off = slot % Bp;
+                if (blk >= num_blocks) { rc = -2; break; }
+                size_t krow = (((size_t)blk * Hkv + h) * Bp + off) * D;
+                double dot = 0.0;
+                for (int32_t d = 0; d < D; ++d) dot += elem(q, dtype, q_off + d) * elem(kpool, dtype, krow + d);
+                x[i - lo] = scale * dot;
+            }
+            if (!rc) {
+                /* softmax over the window, then the weighted sum of V */
+                double m = x[0];
+                for (int64_t i = 1; i < n - lo; ++i) if (x[i] > m) m = x[i];
+                double denom = 0.0;
+                for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+                for (int64_t i = lo; i < n; ++i) {
+                    double w = exp(x[i - lo] - m);
+                    denom += w;
+                    int64_t slot;
+                    orc_physical_slot(table, max_blocks, Bp, i, &slot);
+                    int64_t blk = slot / Bp, off = slot % Bp;
+                    size_t vrow = (((size_t)blk * Hkv + h) * Bp + off) * D;
+                    for (int32_t d = 0; d < D; ++d) o[d] += w * elem(vpool, dtype, vrow + d);
+                }
+                for (int32_t d = 0; d < D; ++d) o[d] /= denom;
+            } else {
+#pragma omp atomic write
+                err = rc;
+            }
+        }
+        free(x);
+    }
+    return err;
+}

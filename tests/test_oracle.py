@@ -401,3 +401,56 @@ def test_shared_prefix_scenario_small():
     ka, _ = wl.kv_values(0, 0, P + 4)
     kb, _ = wl.kv_values(1, 0, P + 4)
     assert torch.equal(ka[:P], kb[:P]) and not torch.equal(ka[P:], kb[P:])
+
+
+# ----------------------------------------------------------------- sliding window
+WINDOW_CASES = [
+    ("f32", 2, 2, 64, 4, [1, 4, 5, 17, 40]),
+    ("bf16", 4, 2, 128, 16, [1, 16, 17, 40, 70]),
+    ("bf16", 8, 1, 128, 1, [33, 2, 9]),
+]
+
+
+@pytest.mark.parametrize("dtype,G,Hkv,D,bp,lens", WINDOW_CASES)
+@pytest.mark.parametrize("window", [1, 3, 16, 17])
+def test_window_decode_matches_library_sdpa_over_the_last_keys(dtype, G, Hkv, D, bp, lens, window):
+    # "03｜PagedAttention 与 KV Cache 内存系统" §7: the window of position p is [p - w + 1, p]
+    wl, oc, q = _small_case(dtype, G, Hkv, D, bp, lens, seed=window + len(lens))
+    got = oracle.decode_window(oc.k, oc.v, q, oc.tables, wl.total_lens, wl.scale, window)
+    qf = oracle.bits_to_f64(q)
+    for s, n in enumerate(wl.total_lens):
+        k, v = _gathered(oc, s, int(n))
+        lo = max(0, int(n) - window)
+        for g in range(wl.num_q_heads):
+            h = g // G
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(qf[s, g][None, None, None]),
+                torch.from_numpy(k[lo:, h][None, None]),
+                torch.from_numpy(v[lo:, h][None, None]), scale=wl.scale)[0, 0, 0].numpy()
+            np.testing.assert_allclose(got[s, g], ref, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("window", [0, -1, 70, 1000])
+def test_window_wider_than_the_context_is_full_decode_bit_for_bit(window):
+    wl, oc, q = _small_case("bf16", 4, 2, 128, 16, [1, 16, 17, 40, 70], seed=5)
+    full = oracle.decode(oc.k, oc.v, q, oc.tables, wl.total_lens, wl.scale)
+    got = oracle.decode_window(oc.k, oc.v, q, oc.tables, wl.total_lens, wl.scale, window)
+    assert np.array_equal(got, full)
+
+
+def test_window_of_one_returns_the_newest_value_exactly():
+    wl, oc, q = _small_case("f32", 2, 2, 64, 4, [1, 5, 17], seed=8)
+    got = oracle.decode_window(oc.k, oc.v, q, oc.tables, wl.total_lens, wl.scale, 1)
+    for s, n in enumerate(wl.total_lens):
+        _, v = _gathered(oc, s, int(n))
+        for g in range(wl.num_q_heads):
+            assert np.array_equal(got[s, g], v[int(n) - 1, g // 2])
+
+
+def test_window_rows_match_full_window_result():
+    wl, oc, q = _small_case("bf16", 4, 2, 128, 16, [40, 70], seed=6)
+    full = oracle.decode_window(oc.k, oc.v, q, oc.tables, wl.total_lens, wl.scale, 20)
+    rows = [(1, 7), (0, 0), (1, 3)]
+    got = oracle.decode_window(oc.k, oc.v, q, oc.tables, wl.total_lens, wl.scale, 20, rows=rows)
+    for r, (s, g) in enumerate(rows):
+        assert np.array_equal(got[r], full[s, g])
