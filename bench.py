@@ -8,9 +8,11 @@ block tables.  The default workload is the GQA decode batch (64 sequences,
 H_q 32 / H_kv 8, head_dim 128, block size 16, bf16, contexts U[128, 4096]).
 ``--workload prefill`` times pa_write_kv + pa_prefill instead.
 
-Timing: W untimed warm-up steps; then K steps, each preceded (outside its
-events) by a 256 MiB write that flushes L2, each bracketed by CUDA events on
-the launching stream; barrier + synchronize around the loop; max over ranks.
+Timing: W untimed warm-up steps; then K steps bracketed by CUDA events on the
+launching stream (the step's K/V is larger than L2; ``--l2 flush`` adds a
+256 MiB write before every step, outside its events); barrier + synchronize
+around the loop; max over ranks.  ``--path fused`` times pa_decode_step (one
+launch) and ``--window W`` pa_decode_window (sliding window) instead.
 value = algorithmic bytes of all ranks / max step time (GB/s).  The
 algorithmic bytes of a decode step are the K/V rows of every visible token,
 Q, the fp32 output, the block-table entries and context lengths.
@@ -59,6 +61,8 @@ def parse():
                     help="decode step: split = pa_write_kv + pa_decode_partial + pa_decode_merge "
                          "(dependent launches; fastest on large batches); fused = pa_decode_step "
                          "(write + attention + merge in one launch; fastest on small batches)")
+    ap.add_argument("--window", type=int, default=0,
+                    help="decode: sliding window in positions (pa_decode_window); 0 = none")
     ap.add_argument("--partition-tokens", type=int, default=0,
                     help="split-KV partition size for decode (0 = the library's choice)")
     return ap.parse_args()
@@ -73,12 +77,14 @@ def measured_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-def algorithmic_bytes(wl) -> dict:
-    """Bytes one decode (or prefill) step must move at minimum."""
+def algorithmic_bytes(wl, window: int = 0) -> dict:
+    """Bytes one decode (or prefill) step must move at minimum (with a sliding
+    window: only the last `window` positions and the pages holding them)."""
     e = wl.elem_bytes
     n = wl.total_lens.astype(np.int64)
-    kv = int(n.sum()) * wl.logical_bytes_per_token()
-    tables = int((-(-n // wl.block_size)).sum()) * 4
+    lo = np.maximum(n - window, 0) if window > 0 else np.zeros_like(n)
+    kv = int((n - lo).sum()) * wl.logical_bytes_per_token()
+    tables = int((-(-n // wl.block_size) - lo // wl.block_size).sum()) * 4
     n_q = int(wl.new_lens.sum())
     q = n_q * wl.num_q_heads * wl.head_dim * e
     out = n_q * wl.num_q_heads * wl.head_dim * 4
@@ -88,8 +94,8 @@ def algorithmic_bytes(wl) -> dict:
             "decode_total": kv + q + out + tables + lens}
 
 
-def ab_kv_mb(wl) -> float:
-    return algorithmic_bytes(wl)["kv"] / 1e6
+def ab_kv_mb(wl, window: int = 0) -> float:
+    return algorithmic_bytes(wl, window)["kv"] / 1e6
 
 
 def prefill_flops(wl) -> float:
@@ -303,7 +309,10 @@ def run_ours(args, rank, world, local_rank):
         g.set_partition_tokens(args.partition_tokens)
     stream = torch.cuda.current_stream(dev)
     is_decode = wl.kind == "decode"
-    fused = is_decode and args.path == "fused"
+    window = args.window if is_decode else 0
+    if window > 0:
+        g.set_window(window)
+    fused = is_decode and args.path == "fused" and window == 0
     max_parts = g.max_parts()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -312,7 +321,7 @@ def run_ours(args, rank, world, local_rank):
             g.step(stream, fused=True)
             return
         g.write_new(stream)
-        if is_decode:
+        if is_decode and window == 0:
             g.attend(stream, "partial")
             g.attend(stream, "merge")
         else:
@@ -363,7 +372,7 @@ def run_ours(args, rank, world, local_rank):
             continue
         g.write_new(stream)
         e[1].record(stream)
-        if is_decode:
+        if is_decode and window == 0:
             g.attend(stream, "partial")
             e[2].record(stream)
             g.attend(stream, "merge")
@@ -384,7 +393,7 @@ def run_ours(args, rank, world, local_rank):
     e2e = run_e2e(args, g, stream, dev, is_decode, fused)
 
     hbm_peak, tf_peak, peak_src = measured_peaks()
-    ab = algorithmic_bytes(wl)
+    ab = algorithmic_bytes(wl, window)
     res = {"metric": METRIC, "n_gpus": world, "steps": K, "warmup": args.warmup,
            "ms_per_step": ms, "scaling": "weak", "vs_baseline": None, "data": "synthetic",
            "dtype": wl.dtype}
@@ -398,8 +407,9 @@ def run_ours(args, rank, world, local_rank):
            "l2": ("flushed before every timed step by a 256 MiB write outside the step's events"
                   if do_flush else
                   "no flush: inputs larger than L2 (the step reads %.0f MB of K/V, L2 is 129 MB)"
-                  % (ab_kv_mb(wl))),
+                  % (ab_kv_mb(wl, window))),
            "split_kv_partitions_max": max_parts,
+           "window": window or "none",
            "path": ("fused: pa_decode_step (new-token write, attention and split-KV merge in one "
                     "launch)" if fused else
                     "split: pa_write_kv + pa_decode_partial + pa_decode_merge" if is_decode else
@@ -419,14 +429,18 @@ def run_ours(args, rank, world, local_rank):
                            "bound": "hbm",
                            "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                            "frac": achieved / hbm_peak, "peak_source": peak_src + " hbm_gbs",
-                           "traffic": recorded_traffic(kname, wl.name),
+                           "traffic": None if window else recorded_traffic(kname, wl.name),
                            "algorithmic_bytes": per_rank, "launch_ms": part_ms}
         if fused:
             res["kernel_ms"] = {"decode_step": part_ms}
             launches = K
         else:
-            res["kernel_ms"] = {"write_kv": float(write_ms.mean()), "decode_partition": part_ms,
-                                "decode_merge": float(merge_ms.mean())}
+            if window:
+                res["kernel_ms"] = {"write_kv": float(write_ms.mean()),
+                                    "decode_window (partition + merge)": part_ms}
+            else:
+                res["kernel_ms"] = {"write_kv": float(write_ms.mean()), "decode_partition": part_ms,
+                                    "decode_merge": float(merge_ms.mean())}
             launches = K * (2 + (1 if max_parts > 1 else 0))
     else:
         flops = prefill_flops(wl)
@@ -494,7 +508,7 @@ def run_e2e(args, g, stream, dev, is_decode, fused=False):
     torch.cuda.synchronize(dev)
     t = float(np.mean([a.elapsed_time(b) for a, b in ms]))
     if is_decode:
-        val, unit = algorithmic_bytes(wl)["decode_total"] / (t * 1e-3) / 1e9, "GB/s"
+        val, unit = algorithmic_bytes(wl, g.window)["decode_total"] / (t * 1e-3) / 1e9, "GB/s"
     else:
         val, unit = prefill_flops(wl) / (t * 1e-3) / 1e12, "TFLOP/s"
     return {"value": val, "unit": unit, "ms_per_step": t, "h2d_bytes_per_step": int(h2d),

@@ -12,8 +12,9 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from paged_kv_cache_148_gb300 import (decode, decode_step, decode_step_workspace,
-                                      decode_workspace_bytes, prefill, write_kv)
+from paged_kv_cache_148_gb300 import (decode, decode_step, decode_step_workspace, decode_window,
+                                      decode_window_workspace_bytes, decode_workspace_bytes,
+                                      prefill, write_kv)
 from paged_kv_cache_148_gb300.cache import PagedCache
 
 WRITE_CHUNK = 32768  # tokens per host->device batch while filling the cache
@@ -92,14 +93,20 @@ class GpuWorkload:
             self.out = torch.empty((int(wl.new_lens.sum()), wl.num_q_heads, wl.head_dim),
                                    dtype=torch.float32, device=self.device)
         self.partition_tokens = 0
+        self.window = 0  # decode: sliding window in positions (0 = the whole context)
         self._alloc_workspace()
 
     def _alloc_workspace(self):
         if self.wl.kind != "decode":
             self.workspace = self.step_workspace = None
             return
-        nb = decode_workspace_bytes(self.cache.pool, self.wl.num_seqs, self.wl.num_q_heads,
-                                    self.max_context, self.partition_tokens)
+        if self.window > 0:
+            nb = decode_window_workspace_bytes(self.cache.pool, self.wl.num_seqs,
+                                               self.wl.num_q_heads, self.max_context, self.window,
+                                               self.partition_tokens)
+        else:
+            nb = decode_workspace_bytes(self.cache.pool, self.wl.num_seqs, self.wl.num_q_heads,
+                                        self.max_context, self.partition_tokens)
         self.workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=self.device)
         # pa_decode_step: zero-filled once, its semaphores return to zero every call
         self.step_workspace = decode_step_workspace(self.cache.pool, self.wl.num_seqs,
@@ -110,12 +117,24 @@ class GpuWorkload:
         self.partition_tokens = int(n)
         self._alloc_workspace()
 
+    def set_window(self, w: int):
+        """Decode attends only to the last w positions (pa_decode_window); 0 = all."""
+        self.window = int(w)
+        self._alloc_workspace()
+
     def write_new(self, stream=None):
         write_kv(self.cache.pool, self.k_new, self.v_new, self.slot_mapping, d_err=self.err,
                  stream=stream)
 
     def attend(self, stream=None, phase: str = "all"):
         wl = self.wl
+        if wl.kind == "decode" and self.window > 0:
+            if phase != "all":
+                raise ValueError("a windowed decode runs as one call")
+            return decode_window(self.cache.pool, self.q, self.block_tables, self.context_lens,
+                                 self.max_context, self.window, wl.scale, out=self.out,
+                                 workspace=self.workspace, partition_tokens=self.partition_tokens,
+                                 d_err=self.err, stream=stream)
         if wl.kind == "decode":
             return decode(self.cache.pool, self.q, self.block_tables, self.context_lens,
                           self.max_context, wl.scale, out=self.out, workspace=self.workspace,

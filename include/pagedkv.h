@@ -232,6 +232,27 @@ pa_status pa_decode_noalloc(const pa_kv_pool* pool, const void* q, int32_t num_q
                             pa_stream_t stream);
 
 /*
+ * Sliding-window decode ("03｜PagedAttention 与 KV Cache 内存系统" §1.1 and §7:
+ * a sliding/local-attention layer uses only the tokens of its window, and the
+ * window of the token at position p is [p - w + 1, p]).  As pa_decode, but the
+ * query of sequence s (position n - 1, n = context_lens[s]) attends only to
+ * positions max(0, n - window) .. n - 1; pages before the window are not read.
+ * window must be >= 1 (else PA_ERR_INVALID_ARG).  The workspace size depends on
+ * the window: pa_decode_window_workspace_bytes.  Other arguments, limits and
+ * errors as pa_decode.
+ */
+pa_status pa_decode_window_workspace_bytes(const pa_kv_pool* pool, int32_t num_seqs,
+                                           int32_t num_q_heads, int32_t max_context,
+                                           int32_t window, int32_t partition_tokens,
+                                           size_t* bytes);
+pa_status pa_decode_window(const pa_kv_pool* pool, const void* q, int32_t num_q_heads,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, int32_t num_seqs, int32_t max_context,
+                           int32_t window, float scale, int32_t partition_tokens, float* out,
+                           void* workspace, size_t workspace_bytes, int32_t* d_err,
+                           pa_stream_t stream);
+
+/*
  * One decode step in a single launch: the fused form of pa_write_kv of one
  * new token per sequence followed by pa_decode (P1 §4.1: the new K/V go to
  * their slots, then attention reads them through the table; P1 §4: split-KV

@@ -41,6 +41,7 @@ EXPORTED = [
     "pa_physical_slot", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks",
     "pa_decode_partition_tokens", "pa_decode_workspace_bytes", "pa_decode", "pa_decode_partial",
     "pa_decode_merge", "pa_decode_noalloc", "pa_decode_step_workspace_bytes", "pa_decode_step",
+    "pa_decode_window_workspace_bytes", "pa_decode_window",
     "pa_prefill",
     "pa_alloc_create", "pa_alloc_destroy", "pa_alloc_append", "pa_alloc_fork",
     "pa_alloc_writable_tail", "pa_alloc_reserve", "pa_alloc_release", "pa_alloc_refcount",
@@ -97,6 +98,8 @@ def lib() -> ctypes.CDLL:
         "pa_decode_merge": ([P, i32, P, i32, i32, i32, P, P, sz, P], i32),
         "pa_decode_noalloc": ([P, P, i32, P, i32, P, i32, i32, f32, i32, P, P, P], i32),
         "pa_decode_step_workspace_bytes": ([P, i32, i32, i32, i32, P], i32),
+        "pa_decode_window_workspace_bytes": ([P, i32, i32, i32, i32, i32, P], i32),
+        "pa_decode_window": ([P, P, i32, P, i32, P, i32, i32, i32, f32, i32, P, P, sz, P, P], i32),
         "pa_decode_step": ([P, P, P, P, P, i32, P, i32, P, i32, i32, f32, i32, P, P, sz, P, P], i32),
         "pa_prefill": ([P, P, i32, i32, P, P, P, i32, i32, i32, i32, f32, i32, P, P, P], i32),
         "pa_alloc_create": ([i32, P, P], i32),
@@ -280,6 +283,42 @@ def decode(pool: KVPool, q: torch.Tensor, block_tables: torch.Tensor, context_le
               _ptr(context_lens), B, int(max_context), float(scale), int(partition_tokens),
               _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_err), _stream(stream)),
            "pa_decode" if phase == "all" else "pa_decode_partial")
+    return out
+
+
+def decode_window_workspace_bytes(pool: KVPool, num_seqs: int, num_q_heads: int,
+                                  max_context: int, window: int, partition_tokens: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().pa_decode_window_workspace_bytes(pool.c, num_seqs, num_q_heads, max_context,
+                                                  int(window), partition_tokens,
+                                                  ctypes.byref(out)),
+           "pa_decode_window_workspace_bytes")
+    return out.value
+
+
+def decode_window(pool: KVPool, q: torch.Tensor, block_tables: torch.Tensor,
+                  context_lens: torch.Tensor, max_context: int, window: int, scale: float,
+                  out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                  partition_tokens: int = 0, d_err: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
+    """Sliding-window paged decode: the query at position n-1 attends to the last
+    `window` positions; returns out [B][H_q][D] float32."""
+    _need(q, "q", pool.dtype, pool.device)
+    _need(block_tables, "block_tables", torch.int32, pool.device)
+    _need(context_lens, "context_lens", torch.int32, pool.device)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=pool.device)
+    _need(out, "out", torch.float32, pool.device)
+    need = decode_window_workspace_bytes(pool, B, Hq, max_context, window, partition_tokens)
+    if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=pool.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode_window(pool.c, _ptr(q), Hq, _ptr(block_tables),
+                                  int(block_tables.shape[1]), _ptr(context_lens), B,
+                                  int(max_context), int(window), float(scale),
+                                  int(partition_tokens), _ptr(out), _ptr(workspace), ws_bytes,
+                                  _ptr(d_err), _stream(stream)), "pa_decode_window")
     return out
 
 

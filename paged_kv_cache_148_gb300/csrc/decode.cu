@@ -37,6 +37,7 @@
 //    (sequence, kv-head) to finish -- counted by a semaphore in the
 //    workspace -- merges the group's partials, so a decode step is one
 //    launch.
+#include <algorithm>
 #include <cfloat>
 #include <cmath>
 
@@ -65,6 +66,8 @@ struct DecodeParams {
     float scale_log2;
     int32_t part_chunks;
     int32_t max_parts;
+    int32_t max_context;
+    int32_t window;               // sliding window in positions (0: the whole context)
     float* out;
     float* ws_m;
     float* ws_l;
@@ -123,10 +126,11 @@ struct DecodeSmem {
 
 // Producer side: lane 0 of a warp fetches chunk `c` (16 tokens starting at
 // c*16) of sequence s, kv-head h, into ring stage `kst` (K) / `kst +
-// kChunkBytes` (V).  Writes the valid-row mask, then arms the barrier.
+// kChunkBytes` (V).  Writes the mask of rows in [lo, n), then arms the barrier.
 template <int W>
-PA_DEVICE void issue_chunk(const DecodeParams& p, int s, int h, int n, int c, int32_t id_first,
-                           unsigned char* kst, uint64_t* bar, uint32_t* mask_slot) {
+PA_DEVICE void issue_chunk(const DecodeParams& p, int s, int h, int n, int lo, int c,
+                           int32_t id_first, unsigned char* kst, uint64_t* bar,
+                           uint32_t* mask_slot) {
     const int t0 = c * kChunk;
     const int bp = 1 << p.log2_bp;
     const int valid = min(kChunk, n - t0);
@@ -141,6 +145,7 @@ PA_DEVICE void issue_chunk(const DecodeParams& p, int s, int h, int n, int c, in
             return;
         }
         mask = (1u << valid) - 1u;  // valid <= 16
+        if (lo > t0) mask &= ~((1u << (lo - t0)) - 1u);  // rows before the window
         bytes = 2 * kChunkBytes;
         const int64_t row0 = ((int64_t)id * p.num_kv_heads + h) * page_rows + (t0 & (bp - 1));
         *mask_slot = mask;
@@ -159,6 +164,7 @@ PA_DEVICE void issue_chunk(const DecodeParams& p, int s, int h, int n, int c, in
         ids[pp] = -1;
         const int tok = t0 + pp * bp;
         if (tok >= n) break;
+        if (tok + bp <= lo) continue;  // the whole page is before the window
         const int e = e0 + pp;
         const int32_t id = (e < p.max_blocks) ? __ldg(table + e) : -1;
         if (e >= p.max_blocks || id >= p.num_blocks) {
@@ -174,6 +180,7 @@ PA_DEVICE void issue_chunk(const DecodeParams& p, int s, int h, int n, int c, in
         mask |= ((1u << rows) - 1u) << (pp * bp);
         bytes += 2u * (uint32_t)bp * kRowBytes;
     }
+    if (lo > t0) mask &= ~((1u << (lo - t0)) - 1u);  // rows before the window
     *mask_slot = mask;
     mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll 1
@@ -287,7 +294,6 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
     using R = Row<T>;
     constexpr int EPL = R::N;                 // elements of a row per lane
     constexpr int D = EPL * 16;               // head_dim
-    constexpr int LOG2G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
     constexpr int NS = 8 * G;                 // partial scores per lane: 8 rows x G heads
     constexpr int ROUNDS = G == 1 ? 3 : 4;    // halving rounds of the transpose-reduce
     constexpr int NSF = G == 1 ? 1 : G / 2;   // finished scores per lane
@@ -297,28 +303,36 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
     const int s = blockIdx.x, h = blockIdx.y, part = blockIdx.z;
     griddep_wait();  // K/V rows, tables and lengths may come from the previous kernel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c_begin = part * p.part_chunks;
-    const int first = c_begin + warp;  // this warp's chunks: first + i*W
     const bool big_pages = p.log2_bp >= 4;
     const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks;
-    // block-table prefetch, issued together with the length load below: lane j
-    // holds the id of local chunk (base + j); entries past the sequence are
-    // in the table row and never used
-    auto table_id = [&](int i) -> int32_t {
-        const int c = first + i * W;
+    auto table_id_at = [&](int c) -> int32_t {
         const int e = (c * kChunk) >> p.log2_bp;
         return e < p.max_blocks ? __ldg(table + e) : -1;
     };
-    int32_t id_reg = big_pages ? table_id(lane) : -1;
+    // With a sliding window only positions lo .. n-1 are visible (the window of
+    // the query at n - 1); partitions then start at chunk c_lo = lo / 16.
+    // Block-table prefetch: lane j holds the id of this warp's local chunk j;
+    // without a window it goes out together with the length load.
+    int32_t id_reg = -1;
+    if (p.window <= 0 && big_pages) id_reg = table_id_at(part * p.part_chunks + warp + lane * W);
     int n = __ldg(p.context_lens + s);
-    if (n > p.max_parts * p.part_chunks * kChunk) {  // longer than the plan's max_context
+    if (n > p.max_context) {  // longer than the plan allows
         if (part == 0 && h == 0 && threadIdx.x == 0) set_error(p.d_err, PA_ERR_OUT_OF_RANGE);
-        n = p.max_parts * p.part_chunks * kChunk;
+        n = p.max_context;
     }
+    int c_lo = 0;
+    if (p.window > 0) {
+        if (n > p.window) c_lo = (n - p.window) / kChunk;
+        if (big_pages) id_reg = table_id_at(c_lo + part * p.part_chunks + warp + lane * W);
+    }
+    const int lo = (p.window > 0 && n > p.window) ? n - p.window : 0;
+    const int c_begin = c_lo + part * p.part_chunks;
+    const int first = c_begin + warp;  // this warp's chunks: first + i*W
+    auto table_id = [&](int i) -> int32_t { return table_id_at(first + i * W); };
     const int n_chunks = (n + kChunk - 1) / kChunk;
     if (n <= 0 || c_begin >= n_chunks) return;
     const int c_end = min(c_begin + p.part_chunks, n_chunks);
-    const int n_parts = (n_chunks + p.part_chunks - 1) / p.part_chunks;
+    const int n_parts = (n_chunks - c_lo + p.part_chunks - 1) / p.part_chunks;
 
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem + (size_t)warp * S * 2 * kChunkBytes;
@@ -343,7 +357,7 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
         const int stage = i % S;
         const int c = first + i * W;
         if (big_pages && ((c * kChunk) >> p.log2_bp) >= p.max_blocks) id = p.num_blocks;  // flagged
-        issue_chunk<W>(p, s, h, n, c, id, ring + (size_t)stage * 2 * kChunkBytes, &bars[stage],
+        issue_chunk<W>(p, s, h, n, lo, c, id, ring + (size_t)stage * 2 * kChunkBytes, &bars[stage],
                        &masks[stage]);
     };
 
@@ -694,10 +708,11 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     const int s = blockIdx.x / p.num_q_heads;
     const int g = blockIdx.x - s * p.num_q_heads;
     griddep_wait();  // partials come from the partition kernel
-    const int n = __ldg(p.context_lens + s);
+    const int n = min(__ldg(p.context_lens + s), p.max_context);
     if (n <= 0) return;
     const int n_chunks = (n + kChunk - 1) / kChunk;
-    const int n_parts = min((n_chunks + p.part_chunks - 1) / p.part_chunks, p.max_parts);
+    const int c_lo = (p.window > 0 && n > p.window) ? (n - p.window) / kChunk : 0;
+    const int n_parts = min((n_chunks - c_lo + p.part_chunks - 1) / p.part_chunks, p.max_parts);
     if (n_parts <= 1) return;
     __shared__ float wts[kMergeMaxParts];
     __shared__ float red[kMergeThreads / 32];
@@ -757,9 +772,11 @@ struct Plan {
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static pa_status make_plan(const pa_kv_pool* pool, int32_t B, int32_t Hq, int32_t max_ctx,
-                           int32_t partition_tokens, Plan* plan) {
-    if (B < 0 || Hq <= 0 || max_ctx < 0) return PA_ERR_INVALID_ARG;
-    const int64_t chunks_max = ((int64_t)max_ctx + kChunk - 1) / kChunk;
+                           int32_t partition_tokens, Plan* plan, int32_t window = 0) {
+    if (B < 0 || Hq <= 0 || max_ctx < 0 || window < 0) return PA_ERR_INVALID_ARG;
+    int64_t chunks_max = ((int64_t)max_ctx + kChunk - 1) / kChunk;
+    // a window of w positions starting anywhere touches at most ceil(w/16) + 1 chunks
+    if (window > 0) chunks_max = std::min<int64_t>(chunks_max, ((int64_t)window + kChunk - 1) / kChunk + 1);
     int64_t pc;
     if (partition_tokens > 0) {
         if (partition_tokens % kChunk != 0) return PA_ERR_INVALID_ARG;
@@ -863,13 +880,12 @@ extern "C" pa_status pa_decode_workspace_bytes(const pa_kv_pool* pool, int32_t n
     return PA_OK;
 }
 
-extern "C" pa_status pa_decode_partial(const pa_kv_pool* pool, const void* q,
-                                       int32_t num_q_heads, const int32_t* block_tables,
-                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
-                                       int32_t num_seqs, int32_t max_context, float scale,
-                                       int32_t partition_tokens, float* out, void* workspace,
-                                       size_t workspace_bytes, int32_t* d_err,
-                                       pa_stream_t stream) {
+static pa_status decode_partial_impl(const pa_kv_pool* pool, const void* q, int32_t num_q_heads,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* context_lens, int32_t num_seqs,
+                                     int32_t max_context, int32_t window, float scale,
+                                     int32_t partition_tokens, float* out, void* workspace,
+                                     size_t workspace_bytes, int32_t* d_err, pa_stream_t stream) {
     pa_status st = check_pool(pool);
     if (st != PA_OK) return st;
     if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq < 0 || max_context < 0)
@@ -885,14 +901,14 @@ extern "C" pa_status pa_decode_partial(const pa_kv_pool* pool, const void* q,
     if (!aligned16(q) || !aligned16(out) || !aligned16(pool->k_pool) || !aligned16(pool->v_pool))
         return PA_ERR_INVALID_ARG;
     Plan plan;
-    st = make_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan);
+    st = make_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan, window);
     if (st != PA_OK) return st;
     if (plan.max_parts > 65535) return PA_ERR_UNSUPPORTED;
     if (plan.ws_bytes > 0 && (workspace == nullptr || workspace_bytes < plan.ws_bytes ||
                               !aligned16(workspace)))
         return PA_ERR_INVALID_ARG;
 
-    DecodeParams prm;
+    DecodeParams prm = {};
     prm.k_pool = static_cast<const unsigned char*>(pool->k_pool);
     prm.v_pool = static_cast<const unsigned char*>(pool->v_pool);
     prm.num_blocks = pool->num_blocks;
@@ -906,6 +922,8 @@ extern "C" pa_status pa_decode_partial(const pa_kv_pool* pool, const void* q,
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.part_chunks = plan.part_chunks;
     prm.max_parts = plan.max_parts;
+    prm.max_context = max_context;
+    prm.window = window;
     prm.out = out;
     bind_workspace(plan, workspace, &prm);
     prm.d_err = d_err;
@@ -915,18 +933,18 @@ extern "C" pa_status pa_decode_partial(const pa_kv_pool* pool, const void* q,
     return dispatch_group<uint16_t, false>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
 }
 
-extern "C" pa_status pa_decode_merge(const pa_kv_pool* pool, int32_t num_q_heads,
-                                     const int32_t* context_lens, int32_t num_seqs,
-                                     int32_t max_context, int32_t partition_tokens, float* out,
-                                     void* workspace, size_t workspace_bytes,
-                                     pa_stream_t stream) {
+static pa_status decode_merge_impl(const pa_kv_pool* pool, int32_t num_q_heads,
+                                   const int32_t* context_lens, int32_t num_seqs,
+                                   int32_t max_context, int32_t window, int32_t partition_tokens,
+                                   float* out, void* workspace, size_t workspace_bytes,
+                                   pa_stream_t stream) {
     pa_status st = check_pool(pool);
     if (st != PA_OK) return st;
     if (num_seqs < 0 || num_q_heads <= 0 || max_context < 0) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
     if (!context_lens || !out) return PA_ERR_INVALID_ARG;
     Plan plan;
-    st = make_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan);
+    st = make_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan, window);
     if (st != PA_OK) return st;
     if (plan.max_parts <= 1) return PA_OK;
     if (workspace == nullptr || workspace_bytes < plan.ws_bytes || !aligned16(workspace))
@@ -936,6 +954,8 @@ extern "C" pa_status pa_decode_merge(const pa_kv_pool* pool, int32_t num_q_heads
     prm.context_lens = context_lens;
     prm.part_chunks = plan.part_chunks;
     prm.max_parts = plan.max_parts;
+    prm.max_context = max_context;
+    prm.window = window;
     prm.out = out;
     bind_workspace(plan, workspace, &prm);
     const int D = pool->head_dim;
@@ -946,6 +966,27 @@ extern "C" pa_status pa_decode_merge(const pa_kv_pool* pool, int32_t num_q_heads
         return PA_ERR_CUDA;
     }
     return launch_status();
+}
+
+extern "C" pa_status pa_decode_partial(const pa_kv_pool* pool, const void* q,
+                                       int32_t num_q_heads, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                       int32_t num_seqs, int32_t max_context, float scale,
+                                       int32_t partition_tokens, float* out, void* workspace,
+                                       size_t workspace_bytes, int32_t* d_err,
+                                       pa_stream_t stream) {
+    return decode_partial_impl(pool, q, num_q_heads, block_tables, max_blocks_per_seq,
+                               context_lens, num_seqs, max_context, 0, scale, partition_tokens,
+                               out, workspace, workspace_bytes, d_err, stream);
+}
+
+extern "C" pa_status pa_decode_merge(const pa_kv_pool* pool, int32_t num_q_heads,
+                                     const int32_t* context_lens, int32_t num_seqs,
+                                     int32_t max_context, int32_t partition_tokens, float* out,
+                                     void* workspace, size_t workspace_bytes,
+                                     pa_stream_t stream) {
+    return decode_merge_impl(pool, num_q_heads, context_lens, num_seqs, max_context, 0,
+                             partition_tokens, out, workspace, workspace_bytes, stream);
 }
 
 extern "C" pa_status pa_decode(const pa_kv_pool* pool, const void* q, int32_t num_q_heads,
@@ -1029,6 +1070,7 @@ extern "C" pa_status pa_decode_step(const pa_kv_pool* pool, const void* k_new, c
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.part_chunks = plan.part_chunks;
     prm.max_parts = plan.max_parts;
+    prm.max_context = max_context;
     prm.out = out;
     bind_workspace(plan, workspace, &prm);
     prm.d_err = d_err;
@@ -1042,4 +1084,35 @@ extern "C" pa_status pa_decode_step(const pa_kv_pool* pool, const void* k_new, c
     if (pool->dtype == PA_DTYPE_F32)
         return dispatch_group<float, true>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
     return dispatch_group<uint16_t, true>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
+}
+
+// ---------------------------------------------------------------- sliding window
+extern "C" pa_status pa_decode_window_workspace_bytes(const pa_kv_pool* pool, int32_t num_seqs,
+                                                      int32_t num_q_heads, int32_t max_context,
+                                                      int32_t window, int32_t partition_tokens,
+                                                      size_t* bytes) {
+    pa_status st = check_pool(pool);
+    if (st != PA_OK) return st;
+    if (!bytes || window <= 0) return PA_ERR_INVALID_ARG;
+    Plan plan;
+    st = make_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan, window);
+    if (st != PA_OK) return st;
+    *bytes = plan.ws_bytes;
+    return PA_OK;
+}
+
+extern "C" pa_status pa_decode_window(const pa_kv_pool* pool, const void* q, int32_t num_q_heads,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t num_seqs,
+                                      int32_t max_context, int32_t window, float scale,
+                                      int32_t partition_tokens, float* out, void* workspace,
+                                      size_t workspace_bytes, int32_t* d_err, pa_stream_t stream) {
+    if (window <= 0) return PA_ERR_INVALID_ARG;
+    pa_status st = decode_partial_impl(pool, q, num_q_heads, block_tables, max_blocks_per_seq,
+                                       context_lens, num_seqs, max_context, window, scale,
+                                       partition_tokens, out, workspace, workspace_bytes, d_err,
+                                       stream);
+    if (st != PA_OK) return st;
+    return decode_merge_impl(pool, num_q_heads, context_lens, num_seqs, max_context, window,
+                             partition_tokens, out, workspace, workspace_bytes, stream);
 }
