@@ -718,6 +718,46 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     __shared__ float red[kMergeThreads / 32];
     const int64_t base = ((int64_t)s * p.num_q_heads + g) * p.max_parts;
     const int tid = threadIdx.x;
+    if (n_parts <= kMergeThreads && D <= kMergeThreads) {
+        // one round of loads: thread i holds partition i's max and sum, and every
+        // thread its output element of the first kPre partitions
+        constexpr int kPre = 8;
+        float pre[kPre];
+#pragma unroll
+        for (int u = 0; u < kPre; ++u)
+            pre[u] = (u < n_parts && tid < D) ? p.ws_acc[(base + u) * D + tid] : 0.f;
+        const float mi = tid < n_parts ? p.ws_m[base + tid] : -INFINITY;
+        const float li = tid < n_parts ? p.ws_l[base + tid] : 0.f;
+        float M = mi;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+        if ((tid & 31) == 0) red[tid >> 5] = M;
+        __syncthreads();
+        M = red[0];
+#pragma unroll
+        for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red[w]);
+        const float wi = tid < n_parts ? ex2(mi - M) : 0.f;
+        wts[tid] = wi;
+        float L = li * wi;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+        __syncthreads();  // everyone has read red[] for M; wts complete
+        if ((tid & 31) == 0) red[tid >> 5] = L;
+        __syncthreads();
+        L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMergeThreads / 32; ++w) L += red[w];
+        if (tid < D) {
+            float acc = 0.f;
+#pragma unroll
+            for (int u = 0; u < kPre; ++u) acc = fmaf(pre[u], wts[u], acc);
+            const float* a = p.ws_acc + base * D + tid;
+#pragma unroll 4
+            for (int i = kPre; i < n_parts; ++i) acc = fmaf(a[(int64_t)i * D], wts[i], acc);
+            p.out[((int64_t)s * p.num_q_heads + g) * D + tid] = acc / L;
+        }
+        return;
+    }
     // global max over partitions
     float M = -INFINITY;
     for (int i = tid; i < n_parts; i += kMergeThreads) M = fmaxf(M, p.ws_m[base + i]);
