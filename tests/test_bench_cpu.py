@@ -61,6 +61,23 @@ def test_algorithmic_bytes_decode_gqa():
     assert 5.0e8 < ab["kv"] < 6.2e8       # about 554 MB of K/V per step
 
 
+def test_algorithmic_bytes_with_a_window():
+    wl = workloads.decode_gqa()
+    full = bench.algorithmic_bytes(wl)
+    # a window at least as long as every context moves exactly the full bytes
+    assert bench.algorithmic_bytes(wl, int(wl.total_lens.max())) == full
+    w = 100
+    ab = bench.algorithmic_bytes(wl, w)
+    n = wl.total_lens.astype(np.int64)
+    vis = np.minimum(n, w)
+    assert ab["kv"] == int(vis.sum()) * 2 * 8 * 128 * 2
+    # pages from the one holding position n - w to the one holding n - 1
+    lo = np.maximum(n - w, 0)
+    pages = (n - 1) // 16 - lo // 16 + 1
+    assert ab["tables"] == int(pages.sum()) * 4
+    assert ab["q"] == full["q"] and ab["out"] == full["out"]
+
+
 def test_prefill_flops_matches_closed_form():
     wl = workloads.prefill()
     # 16 sequences, queries at positions 2048..2559 see pos+1 keys
