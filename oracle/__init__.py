@@ -237,7 +237,9 @@ def _dtype_code(arr: np.ndarray) -> int:
         return 0
     if arr.dtype == np.uint16:
         return 1
-    raise TypeError("pool/query arrays must be float32 or uint16 (bf16 bits)")
+    if arr.dtype == np.float64:
+        return 2
+    raise TypeError("pool/query arrays must be float32, uint16 (bf16 bits) or float64")
 
 
 def _tables_array(tables) -> np.ndarray:

@@ -18,7 +18,8 @@
  *     out = sum_i exp(x_i - max_j x_j) V_i / sum_i exp(x_i - max_j x_j)
  *
  * Pool layout read here: K and V pools, each [num_blocks][H_kv][block_size][D]
- * of f32 or bf16 bit patterns (dtype 0 / 1).  A token at logical position p of
+ * of f32 or bf16 bit patterns (dtype 0 / 1), or float64 (dtype 2: FP8 pages
+ * dequantised by oracle/fp8.py; the query is then float64 too).  A token at logical position p of
  * a sequence lives in block table[p / B_p] at offset p mod B_p.
  * GQA mapping (P2 "物理布局" raises it, leaves it open): q-head g reads
  * kv-head g / (H_q / H_kv).
@@ -40,6 +41,7 @@
 
 static double elem(const void* base, int dtype, size_t i) {
     if (dtype == 0) return (double)((const float*)base)[i];
+    if (dtype == 2) return ((const double*)base)[i];  /* dequantised FP8 values */
     /* bf16: the upper 16 bits of an IEEE float32 */
     uint32_t bits = (uint32_t)((const uint16_t*)base)[i] << 16;
     float f;
