@@ -203,6 +203,11 @@ def cpu_oracle_run(wl, seconds: float):
     import oracle
     oc = oracle.OracleCache(wl)
     q = oracle.to_numpy_bits(wl.queries())
+    kpool, vpool = oc.k, oc.v
+    if getattr(wl, "kv_format", "native") == "fp8":  # attention over the dequantised pages
+        from oracle import fp8
+        kpool, vpool = fp8.dequantized_pools(*fp8.fp8_pools_from(oc.k, oc.v))
+        q = oracle.bits_to_f64(q)
     t_budget = seconds
     if wl.kind == "decode":
         # sequences in batch order until ~t_budget of work, measured by doing it
@@ -212,7 +217,7 @@ def cpu_oracle_run(wl, seconds: float):
             s = done % wl.num_seqs
             rows = [(s, g) for g in range(wl.num_q_heads)]
             t0 = time.perf_counter()
-            oracle.decode(oc.k, oc.v, q, oc.tables, wl.total_lens, wl.scale, rows=rows)
+            oracle.decode(kpool, vpool, q, oc.tables, wl.total_lens, wl.scale, rows=rows)
             elapsed += time.perf_counter() - t0
             n = int(wl.total_lens[s])
             done_bytes += (n * per_tok + wl.num_q_heads * wl.head_dim * (wl.elem_bytes + 4)
@@ -253,6 +258,11 @@ def reference_steps(wl, warmup: int, steps: int, budget_s: float):
     import oracle
     oc = oracle.OracleCache(wl)
     q = oracle.to_numpy_bits(wl.queries())
+    kpool, vpool = oc.k, oc.v
+    if getattr(wl, "kv_format", "native") == "fp8":  # attention over the dequantised pages
+        from oracle import fp8
+        kpool, vpool = fp8.dequantized_pools(*fp8.fp8_pools_from(oc.k, oc.v))
+        q = oracle.bits_to_f64(q)
     per_tok = wl.logical_bytes_per_token()
     if wl.kind != "decode":
         r = cpu_oracle_run(wl, min(budget_s, 30.0))
@@ -260,7 +270,7 @@ def reference_steps(wl, warmup: int, steps: int, budget_s: float):
         return r
     def one(s):
         rows = [(s, g) for g in range(wl.num_q_heads)]
-        oracle.decode(oc.k, oc.v, q, oc.tables, wl.total_lens, wl.scale, rows=rows)
+        oracle.decode(kpool, vpool, q, oc.tables, wl.total_lens, wl.scale, rows=rows)
         n = int(wl.total_lens[s])
         return (n * per_tok + wl.num_q_heads * wl.head_dim * (wl.elem_bytes + 4)
                 + 4 * (-(-n // wl.block_size)) + 4)

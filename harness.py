@@ -25,7 +25,7 @@ class GpuWorkload:
         self.wl = wl
         self.device = torch.device(device)
         self.cache = PagedCache(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim,
-                                wl.torch_dtype, self.device, wl.free_order)
+                                wl.pool_torch_dtype, self.device, wl.free_order)
         self.sid = [None] * wl.num_seqs
         self.cow_pairs = []
         done = set()

@@ -57,7 +57,9 @@ typedef enum {
 
 typedef enum {
     PA_DTYPE_F32 = 0,          /* IEEE float32 storage and operands */
-    PA_DTYPE_BF16 = 1          /* bfloat16 storage and operands, float32 accumulation */
+    PA_DTYPE_BF16 = 1,         /* bfloat16 storage and operands, float32 accumulation */
+    PA_DTYPE_FP8_E4M3 = 2      /* FP8 E4M3 pages with one float32 scale per (token, kv-head)
+                                  row; new rows arrive as bf16, attention runs in float32 */
 } pa_dtype;
 
 /*
@@ -67,6 +69,16 @@ typedef enum {
  * contiguous elements, one token row is head_dim contiguous elements.  The
  * in-block head-major order is a layout choice the pages leave open; slot
  * semantics are exactly the pages' (slot / B_p, slot mod B_p).
+ *
+ * FP8 pages (dtype PA_DTYPE_FP8_E4M3; the pages leave the format of quantised
+ * pages open -- "KV Cache：容量、布局与生命周期" counts bytes per element in
+ * the page budget): k_pool / v_pool hold E4M3 codes (OCP 8-bit float: sign,
+ * 4 exponent bits with bias 7, 3 mantissa bits, max 448), and k_scale /
+ * v_scale hold float32 [num_blocks][num_kv_heads][block_size], one per row.
+ * A row x of D values is stored as code_d = E4M3(x_d * (448 / amax)) (float32
+ * product, round to nearest even, saturating) with scale = amax / 448, amax =
+ * max |x_d| (an all-zero row stores zeros and scale 0); its value is
+ * decode(code_d) * scale.  k_scale / v_scale are ignored for other dtypes.
  */
 typedef struct {
     void* k_pool;
@@ -76,19 +88,22 @@ typedef struct {
     int32_t num_kv_heads;      /* H_kv */
     int32_t head_dim;          /* D */
     int32_t dtype;             /* pa_dtype */
+    void* k_scale;             /* FP8 only: float32 [num_blocks][num_kv_heads][block_size] */
+    void* v_scale;
 } pa_kv_pool;
 
 /* Human-readable name of a status code (static string). */
 const char* pa_status_str(int32_t status);
 /* Text of the last CUDA error seen by this library on the calling thread. */
 const char* pa_last_cuda_error(void);
-/* ABI version of this header: 1. */
+/* ABI version of this header: 2 (pa_kv_pool gained k_scale / v_scale). */
 int32_t pa_abi_version(void);
 
 /*
  * Bytes of one block for one layer, K and V together:
  * 2 * block_size * num_kv_heads * head_dim * dtype_bytes (P1 §3.1, P4
- * "获取显存块的数量").  Host only.
+ * "获取显存块的数量"), plus 2 * block_size * num_kv_heads * 4 bytes of row
+ * scales for FP8 pages.  Host only.
  */
 pa_status pa_page_size_bytes(const pa_kv_pool* pool, int64_t* bytes);
 

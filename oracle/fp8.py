@@ -83,13 +83,14 @@ def dequantize(codes, scales) -> np.ndarray:
 
 
 def poisoned_fp8_pool(num_blocks: int, num_kv_heads: int, block_size: int, head_dim: int):
-    """K and V code pools [N][H][B_p][D] filled with the NaN code, and their scale
-    pools [N][H][B_p] filled with NaN: a read of an unwritten slot shows up."""
+    """K and V code pools [N][H][B_p][D] and their scale pools [N][H][B_p] with every
+    byte 0xFF (code 0xFF is a NaN, and so are the scales): the same poison as the
+    bf16/f32 pools, so a read of an unwritten slot shows up."""
     shape = (num_blocks, num_kv_heads, block_size, head_dim)
-    kc = np.full(shape, NAN_CODE, dtype=np.uint8)
-    vc = np.full(shape, NAN_CODE, dtype=np.uint8)
-    ks = np.full(shape[:3], np.nan, dtype=np.float32)
-    vs = np.full(shape[:3], np.nan, dtype=np.float32)
+    kc = np.full(shape, 0xFF, dtype=np.uint8)
+    vc = np.full(shape, 0xFF, dtype=np.uint8)
+    ks = np.full(shape[:3], 0xFFFFFFFF, dtype=np.uint32).view(np.float32)
+    vs = np.full(shape[:3], 0xFFFFFFFF, dtype=np.uint32).view(np.float32)
     return kc, vc, ks, vs
 
 
@@ -114,13 +115,17 @@ def fp8_pools_from(kpool, vpool):
     """The FP8 pools that writing the same rows through write_kv_fp8 produces,
     from an oracle pool of float32 or bf16 bits (every slot holds the last row
     written to it, so quantising slot by slot is the same as quantising at
-    write time; unwritten slots hold NaN and stay NaN)."""
+    write time); slots never written (NaN-poisoned rows) keep the poison of
+    poisoned_fp8_pool."""
     from . import bits_to_f64
-    kf = bits_to_f64(kpool).astype(np.float32)
-    vf = bits_to_f64(vpool).astype(np.float32)
-    with np.errstate(invalid="ignore"):
-        kc, ks = quantize_rows(kf)
-        vc, vs = quantize_rows(vf)
+    N, H, Bp, D = kpool.shape
+    kc, vc, ks, vs = poisoned_fp8_pool(N, H, Bp, D)
+    for src, codes, scales in ((kpool, kc, ks), (vpool, vc, vs)):
+        f = bits_to_f64(src).astype(np.float32)
+        written = ~np.isnan(f).any(axis=-1)
+        q, sc = quantize_rows(np.where(written[..., None], f, np.float32(0)))
+        codes[written] = q[written]
+        scales[written] = sc[written]
     return kc, vc, ks, vs
 
 

@@ -35,6 +35,7 @@ PA_ERR_TIMEOUT = 8
 
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
+DTYPE_FP8_E4M3 = 2
 
 EXPORTED = [
     "pa_status_str", "pa_last_cuda_error", "pa_abi_version", "pa_page_size_bytes",
@@ -59,7 +60,8 @@ class pa_kv_pool(ctypes.Structure):
     _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
                 ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("dtype", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p)]
 
 
 _lib = None
@@ -155,35 +157,54 @@ def _need(t: torch.Tensor, name: str, dtype=None, device=None):
 
 # --------------------------------------------------------------------------- pool
 class KVPool:
-    """K and V block pools [num_blocks][num_kv_heads][block_size][head_dim] on one device."""
+    """K and V block pools [num_blocks][num_kv_heads][block_size][head_dim] on one device.
+
+    dtype float32 or bfloat16 stores rows as they are; torch.float8_e4m3fn stores
+    E4M3 codes (uint8 tensors k, v) with one float32 scale per row (k_scale,
+    v_scale [num_blocks][num_kv_heads][block_size]); rows are then written and
+    queried in bfloat16 (``io_dtype``).
+    """
 
     def __init__(self, num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
                  dtype: torch.dtype = torch.bfloat16, device="cuda", k=None, v=None):
-        if dtype not in (torch.float32, torch.bfloat16):
-            raise TypeError("pool dtype must be float32 or bfloat16")
+        fp8 = getattr(torch, "float8_e4m3fn", None)
+        if dtype not in (torch.float32, torch.bfloat16) and (fp8 is None or dtype != fp8):
+            raise TypeError("pool dtype must be float32, bfloat16 or float8_e4m3fn")
         self.num_blocks, self.block_size = int(num_blocks), int(block_size)
         self.num_kv_heads, self.head_dim = int(num_kv_heads), int(head_dim)
         self.dtype = dtype
+        self.is_fp8 = fp8 is not None and dtype == fp8
+        self.io_dtype = torch.bfloat16 if self.is_fp8 else dtype
+        store = torch.uint8 if self.is_fp8 else dtype
         shape = (self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim)
-        self.k = torch.empty(shape, dtype=dtype, device=device) if k is None else k
-        self.v = torch.empty(shape, dtype=dtype, device=device) if v is None else v
+        self.k = torch.empty(shape, dtype=store, device=device) if k is None else k
+        self.v = torch.empty(shape, dtype=store, device=device) if v is None else v
         for t, n in ((self.k, "k"), (self.v, "v")):
-            if tuple(t.shape) != shape or t.dtype != dtype:
+            if tuple(t.shape) != shape or t.dtype != store:
                 raise ValueError("pool tensor %s has the wrong shape or dtype" % n)
             _need(t, "pool." + n)
         self.device = self.k.device
+        self.k_scale = self.v_scale = None
+        if self.is_fp8:
+            self.k_scale = torch.empty(shape[:3], dtype=torch.float32, device=self.device)
+            self.v_scale = torch.empty(shape[:3], dtype=torch.float32, device=self.device)
+        code = DTYPE_FP8_E4M3 if self.is_fp8 else (DTYPE_F32 if dtype == torch.float32
+                                                   else DTYPE_BF16)
         self._c = pa_kv_pool(self.k.data_ptr(), self.v.data_ptr(), self.num_blocks,
-                             self.block_size, self.num_kv_heads, self.head_dim,
-                             DTYPE_F32 if dtype == torch.float32 else DTYPE_BF16)
+                             self.block_size, self.num_kv_heads, self.head_dim, code,
+                             None if self.k_scale is None else self.k_scale.data_ptr(),
+                             None if self.v_scale is None else self.v_scale.data_ptr())
 
     @property
     def c(self):
         return ctypes.byref(self._c)
 
     def poison(self):
-        """Fill both pools with NaN bit patterns (all bytes 0xFF)."""
-        self.k.view(torch.uint8).fill_(0xFF)
-        self.v.view(torch.uint8).fill_(0xFF)
+        """Fill the pools with NaN bit patterns (all bytes 0xFF; for FP8 pages the
+        codes and the scales)."""
+        for t in (self.k, self.v, self.k_scale, self.v_scale):
+            if t is not None:
+                t.view(torch.uint8).fill_(0xFF)
         return self
 
 
@@ -217,8 +238,8 @@ def write_kv(pool: KVPool, k_new: torch.Tensor, v_new: torch.Tensor, slot_mappin
              d_err: Optional[torch.Tensor] = None, stream=None):
     """Scatter k_new/v_new [T][H_kv][D] into the pool at slot_mapping [T] (int64)."""
     T = int(slot_mapping.shape[0])
-    _need(k_new, "k_new", pool.dtype, pool.device)
-    _need(v_new, "v_new", pool.dtype, pool.device)
+    _need(k_new, "k_new", pool.io_dtype, pool.device)
+    _need(v_new, "v_new", pool.io_dtype, pool.device)
     _need(slot_mapping, "slot_mapping", torch.int64, pool.device)
     if tuple(k_new.shape) != (T, pool.num_kv_heads, pool.head_dim) or k_new.shape != v_new.shape:
         raise ValueError("k_new/v_new must be [T][H_kv][D] with T = len(slot_mapping)")
@@ -262,7 +283,7 @@ def decode(pool: KVPool, q: torch.Tensor, block_tables: torch.Tensor, context_le
     phase: "all" (pa_decode), "partial" (pa_decode_partial) or "merge"
     (pa_decode_merge, which needs the workspace the partial phase filled).
     """
-    _need(q, "q", pool.dtype, pool.device)
+    _need(q, "q", pool.io_dtype, pool.device)
     _need(block_tables, "block_tables", torch.int32, pool.device)
     _need(context_lens, "context_lens", torch.int32, pool.device)
     B, Hq, D = q.shape
@@ -303,7 +324,7 @@ def decode_window(pool: KVPool, q: torch.Tensor, block_tables: torch.Tensor,
                   stream=None) -> torch.Tensor:
     """Sliding-window paged decode: the query at position n-1 attends to the last
     `window` positions; returns out [B][H_q][D] float32."""
-    _need(q, "q", pool.dtype, pool.device)
+    _need(q, "q", pool.io_dtype, pool.device)
     _need(block_tables, "block_tables", torch.int32, pool.device)
     _need(context_lens, "context_lens", torch.int32, pool.device)
     B, Hq, D = q.shape
@@ -347,10 +368,10 @@ def decode_step(pool: KVPool, k_new: torch.Tensor, v_new: torch.Tensor, slot_map
 
     workspace comes from decode_step_workspace() (zero-filled once, then reused).
     """
-    _need(k_new, "k_new", pool.dtype, pool.device)
-    _need(v_new, "v_new", pool.dtype, pool.device)
+    _need(k_new, "k_new", pool.io_dtype, pool.device)
+    _need(v_new, "v_new", pool.io_dtype, pool.device)
     _need(slot_mapping, "slot_mapping", torch.int64, pool.device)
-    _need(q, "q", pool.dtype, pool.device)
+    _need(q, "q", pool.io_dtype, pool.device)
     _need(block_tables, "block_tables", torch.int32, pool.device)
     _need(context_lens, "context_lens", torch.int32, pool.device)
     B, Hq, D = q.shape
@@ -375,7 +396,7 @@ def prefill(pool: KVPool, q: torch.Tensor, cu_seqlens_q: torch.Tensor, context_l
             causal: bool = True, out: Optional[torch.Tensor] = None,
             d_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Paged chunked-prefill attention; returns out [T][H_q][D] float32."""
-    _need(q, "q", pool.dtype, pool.device)
+    _need(q, "q", pool.io_dtype, pool.device)
     _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, pool.device)
     _need(context_lens, "context_lens", torch.int32, pool.device)
     _need(block_tables, "block_tables", torch.int32, pool.device)

@@ -47,8 +47,7 @@
 namespace pa {
 
 constexpr int kChunk = 16;                        // tokens per ring stage
-constexpr int kRowBytes = 256;                    // head_dim * element bytes
-constexpr int kChunkBytes = kChunk * kRowBytes;   // 4 KiB of K (and of V) per stage
+constexpr int kRowBytes = 256;                    // bf16 / f32 rows (FP8 rows: 128)
 constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale when max grows > 256x
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -78,20 +77,26 @@ struct DecodeParams {
     const unsigned char* v_new;
     const int64_t* slot_mapping;  // [B] slot of position context_lens[s] - 1
     int32_t* sem;                 // [B][H_kv] partitions finished (zero between calls)
+    // FP8 pages: float row scales [num_blocks][H_kv][B_p]
+    const float* k_scale;
+    const float* v_scale;
 };
 
+// Storage types of a pool row.  A lane owns one column of kColBytes bytes of a
+// row (16 lanes cover a row), which load2 turns into element pairs (float2).
+// Q is read with Row<Q>.  kScaled: the pool carries one float scale per row
+// (FP8 pages), applied to the finished score (K) and folded into the
+// probability (V).
 template <typename T>
 struct Row;
 template <>
 struct Row<float> {
     static constexpr int N = 4;  // elements per 16-byte column
-    static PA_DEVICE void unpack(const uint4& u, float (&f)[4]) {
-        f[0] = __uint_as_float(u.x);
-        f[1] = __uint_as_float(u.y);
-        f[2] = __uint_as_float(u.z);
-        f[3] = __uint_as_float(u.w);
-    }
-    static PA_DEVICE void unpack2(const uint4& u, float2 (&f)[2]) {
+    static constexpr int kRowBytes = 256, kColBytes = 16;
+    static constexpr bool kScaled = false;
+    using Q = float;
+    static PA_DEVICE void load2(const unsigned char* p, float2 (&f)[2]) {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
         f[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
         f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
     }
@@ -99,38 +104,70 @@ struct Row<float> {
 template <>
 struct Row<uint16_t> {  // bf16 bit patterns
     static constexpr int N = 8;
-    static PA_DEVICE void unpack(const uint4& u, float (&f)[8]) {
-        f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
-        f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
-        f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
-        f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
-    }
-    static PA_DEVICE void unpack2(const uint4& u, float2 (&f)[4]) {
+    static constexpr int kRowBytes = 256, kColBytes = 16;
+    static constexpr bool kScaled = false;
+    using Q = uint16_t;
+    static PA_DEVICE void load2(const unsigned char* p, float2 (&f)[4]) {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
         f[0] = make_float2(bf16_lo(u.x), bf16_hi(u.x));
         f[1] = make_float2(bf16_lo(u.y), bf16_hi(u.y));
         f[2] = make_float2(bf16_lo(u.z), bf16_hi(u.z));
         f[3] = make_float2(bf16_lo(u.w), bf16_hi(u.w));
     }
 };
+// two E4M3 codes (low byte first) -> their values, exactly (through f16x2)
+PA_DEVICE float2 e4m3x2_to_float2(uint32_t two) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two));
+    float2 f;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(f.x), "=f"(f.y) : "r"(h2));
+    return f;
+}
+template <>
+struct Row<uint8_t> {  // FP8 E4M3 codes, one float scale per row
+    static constexpr int N = 8;  // elements per 8-byte column
+    static constexpr int kRowBytes = 128, kColBytes = 8;
+    static constexpr bool kScaled = true;
+    using Q = uint16_t;  // queries stay bf16
+    static PA_DEVICE void load2(const unsigned char* p, float2 (&f)[4]) {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        f[0] = e4m3x2_to_float2(u.x & 0xffffu);
+        f[1] = e4m3x2_to_float2(u.x >> 16);
+        f[2] = e4m3x2_to_float2(u.y & 0xffffu);
+        f[3] = e4m3x2_to_float2(u.y >> 16);
+    }
+};
 
-template <int W, int S, int G>
+// Shared memory of a CTA: per warp S ring stages of [K chunk | V chunk |
+// K row scales | V row scales] (the scales only for scaled rows), then the
+// stages' mbarriers and valid-row masks, then the (p, p) probability pairs.
+template <int W, int S, int G, typename R>
 struct DecodeSmem {
-    static constexpr size_t ring = (size_t)W * S * 2 * kChunkBytes;
+    static constexpr int chunk = kChunk * R::kRowBytes;          // K (or V) bytes per stage
+    static constexpr int scales = R::kScaled ? 2 * kChunk * 4 : 0;
+    static constexpr int stage = 2 * chunk + scales;
+    static constexpr size_t ring = (size_t)W * S * stage;
     static constexpr size_t bars = ring;
     static constexpr size_t masks = bars + (size_t)W * S * 8;
     static constexpr size_t probs = masks + (size_t)W * S * 4;
     static constexpr size_t total = probs + (size_t)W * kChunk * G * 8;  // (p, p) pairs
     // the CTA combine reuses the ring: per warp 2G + G*D floats
     static_assert((size_t)W * (4 * G + G * 128) * 4 <= ring, "combine area must fit in the ring");
+    static_assert(stage % 16 == 0, "bulk copy destinations stay 16-byte aligned");
 };
 
 // Producer side: lane 0 of a warp fetches chunk `c` (16 tokens starting at
-// c*16) of sequence s, kv-head h, into ring stage `kst` (K) / `kst +
-// kChunkBytes` (V).  Writes the mask of rows in [lo, n), then arms the barrier.
-template <int W>
+// c*16) of sequence s, kv-head h, into the ring stage at `kst`: K rows, V rows
+// and, for scaled rows, the 16 K and 16 V row scales.  Writes the mask of rows
+// in [lo, n), then arms the barrier with the bytes in flight.
+template <int W, typename R>
 PA_DEVICE void issue_chunk(const DecodeParams& p, int s, int h, int n, int lo, int c,
                            int32_t id_first, unsigned char* kst, uint64_t* bar,
                            uint32_t* mask_slot) {
+    constexpr int RB = R::kRowBytes, CB = kChunk * RB;
+    constexpr uint32_t kScaleBytes = R::kScaled ? 4 : 0;  // per row, for K and for V
     const int t0 = c * kChunk;
     const int bp = 1 << p.log2_bp;
     const int valid = min(kChunk, n - t0);
@@ -146,12 +183,16 @@ PA_DEVICE void issue_chunk(const DecodeParams& p, int s, int h, int n, int lo, i
         }
         mask = (1u << valid) - 1u;  // valid <= 16
         if (lo > t0) mask &= ~((1u << (lo - t0)) - 1u);  // rows before the window
-        bytes = 2 * kChunkBytes;
+        bytes = 2 * CB + 2 * kChunk * kScaleBytes;
         const int64_t row0 = ((int64_t)id * p.num_kv_heads + h) * page_rows + (t0 & (bp - 1));
         *mask_slot = mask;
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(kst, p.k_pool + row0 * kRowBytes, kChunkBytes, bar);
-        bulk_g2s(kst + kChunkBytes, p.v_pool + row0 * kRowBytes, kChunkBytes, bar);
+        bulk_g2s(kst, p.k_pool + row0 * RB, CB, bar);
+        bulk_g2s(kst + CB, p.v_pool + row0 * RB, CB, bar);
+        if constexpr (R::kScaled) {
+            bulk_g2s(kst + 2 * CB, p.k_scale + row0, kChunk * 4, bar);
+            bulk_g2s(kst + 2 * CB + kChunk * 4, p.v_scale + row0, kChunk * 4, bar);
+        }
         return;
     }
     // block size below the chunk: 16 / bp pages per chunk
@@ -178,7 +219,7 @@ PA_DEVICE void issue_chunk(const DecodeParams& p, int s, int h, int n, int lo, i
         ids[pp] = id;
         const int rows = min(bp, n - tok);
         mask |= ((1u << rows) - 1u) << (pp * bp);
-        bytes += 2u * (uint32_t)bp * kRowBytes;
+        bytes += 2u * (uint32_t)bp * (RB + kScaleBytes);
     }
     if (lo > t0) mask &= ~((1u << (lo - t0)) - 1u);  // rows before the window
     *mask_slot = mask;
@@ -188,9 +229,14 @@ PA_DEVICE void issue_chunk(const DecodeParams& p, int s, int h, int n, int lo, i
         if (t0 + pp * bp >= n) break;
         if (ids[pp] < 0) continue;
         const int64_t row0 = ((int64_t)ids[pp] * p.num_kv_heads + h) * page_rows;
-        const uint32_t nb = (uint32_t)bp * kRowBytes;
-        bulk_g2s(kst + pp * bp * kRowBytes, p.k_pool + row0 * kRowBytes, nb, bar);
-        bulk_g2s(kst + kChunkBytes + pp * bp * kRowBytes, p.v_pool + row0 * kRowBytes, nb, bar);
+        const uint32_t nb = (uint32_t)bp * RB;
+        bulk_g2s(kst + pp * bp * RB, p.k_pool + row0 * RB, nb, bar);
+        bulk_g2s(kst + CB + pp * bp * RB, p.v_pool + row0 * RB, nb, bar);
+        if constexpr (R::kScaled) {  // bp >= 4: 16-byte pieces
+            bulk_g2s(kst + 2 * CB + pp * bp * 4, p.k_scale + row0, (uint32_t)bp * 4, bar);
+            bulk_g2s(kst + 2 * CB + kChunk * 4 + pp * bp * 4, p.v_scale + row0, (uint32_t)bp * 4,
+                     bar);
+        }
     }
 }
 
@@ -297,8 +343,10 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
     constexpr int NS = 8 * G;                 // partial scores per lane: 8 rows x G heads
     constexpr int ROUNDS = G == 1 ? 3 : 4;    // halving rounds of the transpose-reduce
     constexpr int NSF = G == 1 ? 1 : G / 2;   // finished scores per lane
-    using L = DecodeSmem<W, S, G>;
+    using L = DecodeSmem<W, S, G, R>;
+    constexpr int RB = R::kRowBytes;          // bytes of a stored row
     static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group size");
+    static_assert(!kFused || RB == 256, "the fused new-row write moves 16 bytes per lane");
 
     const int s = blockIdx.x, h = blockIdx.y, part = blockIdx.z;
     griddep_wait();  // K/V rows, tables and lengths may come from the previous kernel
@@ -335,7 +383,7 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
     const int n_parts = (n_chunks - c_lo + p.part_chunks - 1) / p.part_chunks;
 
     extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char* ring = smem + (size_t)warp * S * 2 * kChunkBytes;
+    unsigned char* ring = smem + (size_t)warp * S * L::stage;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars) + warp * S;
     uint32_t* masks = reinterpret_cast<uint32_t*>(smem + L::masks) + warp * S;
     float2* ps = reinterpret_cast<float2*>(smem + L::probs) + warp * kChunk * G;
@@ -357,8 +405,8 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
         const int stage = i % S;
         const int c = first + i * W;
         if (big_pages && ((c * kChunk) >> p.log2_bp) >= p.max_blocks) id = p.num_blocks;  // flagged
-        issue_chunk<W>(p, s, h, n, lo, c, id, ring + (size_t)stage * 2 * kChunkBytes, &bars[stage],
-                       &masks[stage]);
+        issue_chunk<W, R>(p, s, h, n, lo, c, id, ring + (size_t)stage * L::stage, &bars[stage],
+                          &masks[stage]);
     };
 
     // fused step: the warp that streams the chunk holding position n - 1 loads
@@ -404,13 +452,13 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
     constexpr int EP = EPL / 2;
     float2 q2[G][EP];
     {
-        const T* qb = reinterpret_cast<const T*>(p.q) +
-                      ((int64_t)s * p.num_q_heads + (int64_t)h * G) * D + col * EPL;
+        using QT = typename R::Q;  // the query's storage type (bf16 for FP8 pages)
+        const QT* qb = reinterpret_cast<const QT*>(p.q) +
+                       ((int64_t)s * p.num_q_heads + (int64_t)h * G) * D + col * EPL;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            const uint4 u = __ldg(reinterpret_cast<const uint4*>(qb + (int64_t)(g ^ gx) * D));
             float2 f[EP];
-            R::unpack2(u, f);
+            Row<QT>::load2(reinterpret_cast<const unsigned char*>(qb + (int64_t)(g ^ gx) * D), f);
 #pragma unroll
             for (int e = 0; e < EP; ++e)
                 q2[g][e] = make_float2(f[e].x * p.scale_log2, f[e].y * p.scale_log2);
@@ -442,8 +490,10 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
         }
         const uint32_t vmask = masks[stage];
         const bool masked = vmask != 0xffffu;
-        const unsigned char* kst = ring + (size_t)stage * 2 * kChunkBytes;
-        const unsigned char* vst = kst + kChunkBytes;
+        const unsigned char* kst = ring + (size_t)stage * L::stage;
+        const unsigned char* vst = kst + L::chunk;
+        const float* ksc = reinterpret_cast<const float*>(kst + 2 * L::chunk);  // scaled rows only
+        const float* vsc = ksc + kChunk;
         if (owner && first + i * W == last_chunk) {
             const int pos = n - 1;
             const int64_t bpm = (1 << p.log2_bp) - 1;
@@ -473,9 +523,8 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int row = 2 * (j ^ jx) + half;
-            const uint4 u = *reinterpret_cast<const uint4*>(kst + row * kRowBytes + col * 16);
             float2 k[EP];
-            R::unpack2(u, k);
+            R::load2(kst + row * RB + col * R::kColBytes, k);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 // even and odd elements accumulate in the two halves of a packed FMA
@@ -497,9 +546,11 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
         // ---- online softmax (base 2) with rare rescaling
         const bool tvalid = !masked || ((vmask >> t_mine) & 1u);
         float sc[NSF], mm[NSF];
+        // scaled rows: the K row scale multiplies the finished score
+        const float kscale = (R::kScaled && tvalid) ? ksc[t_mine] : 1.f;
 #pragma unroll
         for (int x = 0; x < NSF; ++x) {
-            sc[x] = tvalid ? part[x] : -INFINITY;
+            sc[x] = tvalid ? part[x] * kscale : -INFINITY;
             mm[x] = G == 1 ? m[0] : ((lane & 1) ? m[G / 2 + x] : m[x]);
         }
         bool need = false;
@@ -549,11 +600,16 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
 
         // ---- broadcast probabilities of the 16 rows x G heads, each stored as a
         //      (p, p) pair so the P*V packed FMAs read their operand directly
+        //      (scaled rows: the V row scale is folded into the pair; l keeps p)
+        const float vscale = R::kScaled ? (tvalid ? vsc[t_mine] : 0.f) : 1.f;
         if (G == 1) {
-            if ((lane & 1) == 0) ps[t_mine] = make_float2(pr[0], pr[0]);
+            if ((lane & 1) == 0) ps[t_mine] = make_float2(pr[0] * vscale, pr[0] * vscale);
         } else {
 #pragma unroll
-            for (int x = 0; x < NSF; ++x) ps[t_mine * G + gx + x] = make_float2(pr[x], pr[x]);
+            for (int x = 0; x < NSF; ++x) {
+                const float pv = pr[x] * vscale;
+                ps[t_mine * G + gx + x] = make_float2(pv, pv);
+            }
         }
         __syncwarp();
 
@@ -564,9 +620,8 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
             float2 pg[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) pg[g] = ps[row * G + g];
-            const uint4 u = *reinterpret_cast<const uint4*>(vst + row * kRowBytes + col * 16);
             float2 v[EP];
-            R::unpack2(u, v);
+            R::load2(vst + row * RB + col * R::kColBytes, v);
             if (masked && !((vmask >> row) & 1u)) {
 #pragma unroll
                 for (int e = 0; e < EP; ++e) v[e] = make_float2(0.f, 0.f);  // unwritten rows may hold NaN
@@ -848,7 +903,7 @@ static pa_status make_plan(const pa_kv_pool* pool, int32_t B, int32_t Hq, int32_
 template <typename T, int G, bool kFused>
 static pa_status launch_partial(const DecodeParams& prm, int32_t B, int32_t Hkv, int32_t max_parts,
                                 cudaStream_t stream) {
-    using Lay = DecodeSmem<kWarps, kStages, G>;
+    using Lay = DecodeSmem<kWarps, kStages, G, Row<T>>;
     auto kern = decode_partition_kernel<T, G, kWarps, kStages, kFused>;
     static bool attr_done[64] = {false};
     int dev = 0;
@@ -935,7 +990,13 @@ static pa_status decode_partial_impl(const pa_kv_pool* pool, const void* q, int3
     if (num_q_heads % pool->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     if (!(scale == scale)) return PA_ERR_INVALID_ARG;
     const int G = num_q_heads / pool->num_kv_heads;
-    if ((int64_t)pool->head_dim * dtype_bytes(pool->dtype) != kRowBytes) return PA_ERR_UNSUPPORTED;
+    const bool fp8 = pool->dtype == PA_DTYPE_FP8_E4M3;
+    if (fp8) {  // bf16 queries against E4M3 rows of D = 128 with float row scales
+        if (pool->head_dim != 128 || pool->block_size < 4) return PA_ERR_UNSUPPORTED;
+        if (!aligned16(pool->k_scale) || !aligned16(pool->v_scale)) return PA_ERR_INVALID_ARG;
+    } else if ((int64_t)pool->head_dim * dtype_bytes(pool->dtype) != kRowBytes) {
+        return PA_ERR_UNSUPPORTED;
+    }
     if (!is_pow2(pool->block_size)) return PA_ERR_UNSUPPORTED;
     if (pool->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(out) || !aligned16(pool->k_pool) || !aligned16(pool->v_pool))
@@ -967,7 +1028,11 @@ static pa_status decode_partial_impl(const pa_kv_pool* pool, const void* q, int3
     prm.out = out;
     bind_workspace(plan, workspace, &prm);
     prm.d_err = d_err;
+    prm.k_scale = fp8 ? static_cast<const float*>(pool->k_scale) : nullptr;
+    prm.v_scale = fp8 ? static_cast<const float*>(pool->v_scale) : nullptr;
     cudaStream_t cs = (cudaStream_t)stream;
+    if (fp8)
+        return dispatch_group<uint8_t, false>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
     if (pool->dtype == PA_DTYPE_F32)
         return dispatch_group<float, false>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
     return dispatch_group<uint16_t, false>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
@@ -1082,6 +1147,7 @@ extern "C" pa_status pa_decode_step(const pa_kv_pool* pool, const void* k_new, c
     if (num_q_heads % pool->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     if (!(scale == scale)) return PA_ERR_INVALID_ARG;
     const int G = num_q_heads / pool->num_kv_heads;
+    if (pool->dtype == PA_DTYPE_FP8_E4M3) return PA_ERR_UNSUPPORTED;  // the step writes raw rows
     if ((int64_t)pool->head_dim * dtype_bytes(pool->dtype) != kRowBytes) return PA_ERR_UNSUPPORTED;
     if (!is_pow2(pool->block_size)) return PA_ERR_UNSUPPORTED;
     if (pool->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;

@@ -67,15 +67,18 @@ const char* pa_status_str(int32_t s) {
 
 const char* pa_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
 
-int32_t pa_abi_version(void) { return 1; }
+int32_t pa_abi_version(void) { return 2; }
 
 pa_status pa_page_size_bytes(const pa_kv_pool* pool, int64_t* bytes) {
     if (!pool || !bytes) return PA_ERR_INVALID_ARG;
     if (pool->block_size <= 0 || pool->num_kv_heads <= 0 || pool->head_dim <= 0)
         return PA_ERR_INVALID_ARG;
-    if (pool->dtype != PA_DTYPE_F32 && pool->dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
+    if (pool->dtype != PA_DTYPE_F32 && pool->dtype != PA_DTYPE_BF16 &&
+        pool->dtype != PA_DTYPE_FP8_E4M3)
+        return PA_ERR_INVALID_ARG;
     *bytes = 2ll * pool->block_size * pool->num_kv_heads * pool->head_dim *
              dtype_bytes(pool->dtype);
+    if (pool->dtype == PA_DTYPE_FP8_E4M3) *bytes += 2ll * pool->block_size * pool->num_kv_heads * 4;
     return PA_OK;
 }
 

@@ -11,7 +11,9 @@ namespace pa {
 // Last CUDA error text seen by this library on the calling thread.
 void record_cuda_error(cudaError_t e);
 
-inline int32_t dtype_bytes(int32_t dtype) { return dtype == PA_DTYPE_F32 ? 4 : 2; }
+inline int32_t dtype_bytes(int32_t dtype) {
+    return dtype == PA_DTYPE_F32 ? 4 : dtype == PA_DTYPE_FP8_E4M3 ? 1 : 2;
+}
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -27,7 +29,10 @@ inline pa_status check_pool(const pa_kv_pool* p) {
     if (p == nullptr || p->k_pool == nullptr || p->v_pool == nullptr) return PA_ERR_INVALID_ARG;
     if (p->num_blocks <= 0 || p->block_size <= 0 || p->num_kv_heads <= 0 || p->head_dim <= 0)
         return PA_ERR_INVALID_ARG;
-    if (p->dtype != PA_DTYPE_F32 && p->dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
+    if (p->dtype != PA_DTYPE_F32 && p->dtype != PA_DTYPE_BF16 && p->dtype != PA_DTYPE_FP8_E4M3)
+        return PA_ERR_INVALID_ARG;
+    if (p->dtype == PA_DTYPE_FP8_E4M3 && (p->k_scale == nullptr || p->v_scale == nullptr))
+        return PA_ERR_INVALID_ARG;
     return PA_OK;
 }
 

@@ -52,7 +52,7 @@ def test_library_is_built_for_sm_103a():
 def test_status_strings(L):
     for code in range(9):
         assert pkv.status_str(code).startswith("PA_")
-    assert L.pa_abi_version() == 1
+    assert L.pa_abi_version() == 2
 
 
 def test_physical_slot_worked_example(L):

@@ -58,6 +58,9 @@ class Workload:
     pair_of: Optional[np.ndarray] = None
     prefix_len: Optional[np.ndarray] = None
     seed_values: int = 0
+    # "native": the pool stores rows in `dtype`; "fp8": E4M3 codes with one float32
+    # scale per (token, kv-head) row, written from the same `dtype` (bf16) rows
+    kv_format: str = "native"
 
     @property
     def torch_dtype(self):
@@ -140,8 +143,15 @@ class Workload:
         return self._draw(g, (n, self.num_q_heads, self.head_dim))
 
     def logical_bytes_per_token(self) -> int:
-        """Bytes of K plus V one token occupies for one layer (all KV heads)."""
+        """Bytes of K plus V one token occupies for one layer (all KV heads);
+        FP8 pages: one byte per element plus a 4-byte scale per row."""
+        if self.kv_format == "fp8":
+            return 2 * self.num_kv_heads * (self.head_dim + 4)
         return 2 * self.num_kv_heads * self.head_dim * self.elem_bytes
+
+    @property
+    def pool_torch_dtype(self):
+        return torch.float8_e4m3fn if self.kv_format == "fp8" else self.torch_dtype
 
 
 def _pool_for(rng, blocks_needed: int, factor: float, minimum: int = 0) -> tuple[int, np.ndarray]:
@@ -216,9 +226,22 @@ def prefill(scale: float = 1.0) -> Workload:
                     cached, new, n_blk, order, seed_values=2005)
 
 
+def with_fp8_pages(wl: Workload) -> Workload:
+    """The same workload (structure and bf16 values) stored in FP8 pages."""
+    if wl.dtype != "bf16":
+        raise ValueError("FP8 pages are written from bf16 rows")
+    return dataclasses.replace(wl, name=wl.name + "_fp8", kv_format="fp8")
+
+
+def decode_gqa_fp8(scale: float = 1.0) -> Workload:
+    """The GQA decode batch with FP8 (E4M3) pages."""
+    return with_fp8_pages(decode_gqa(scale))
+
+
 WORKLOADS = {
     "decode_tiny": decode_tiny,
     "decode_gqa": decode_gqa,
+    "decode_gqa_fp8": decode_gqa_fp8,
     "decode_mha": decode_mha,
     "decode_long_shared": decode_long_shared,
     "prefill": prefill,
