@@ -336,7 +336,7 @@ PA_DEVICE void merge_group(const DecodeParams& p, int s, int h, int n_parts, flo
 }
 
 template <typename T, int G, int W, int S, bool kFused>
-__global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodeParams p) {
+PA_DEVICE void decode_partition_body(const DecodeParams& p) {
     using R = Row<T>;
     constexpr int EPL = R::N;                 // elements of a row per lane
     constexpr int D = EPL * 16;               // head_dim
@@ -751,6 +751,20 @@ __global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodePa
     }
 }
 
+// The partition kernel.  FP8 rows at G <= 4 need half the shared memory of
+// 16-bit rows, so their variant caps registers for 4 resident CTAs per SM;
+// the others keep the compiler's own register choice (3 CTAs per SM by
+// shared memory, 2 at G = 8).
+template <typename T, int G, int W, int S, bool kFused>
+__global__ void __launch_bounds__(W * 32) decode_partition_kernel(const DecodeParams p) {
+    decode_partition_body<T, G, W, S, kFused>(p);
+}
+
+template <typename T, int G, int W, int S>
+__global__ void __launch_bounds__(W * 32, 4) decode_partition_kernel_4ctas(const DecodeParams p) {
+    decode_partition_body<T, G, W, S, false>(p);
+}
+
 // Merge of split-KV partials (P1 §4): M = max m_p, L = sum l_p 2^(m_p - M),
 // out = sum acc_p 2^(m_p - M) / L.  One CTA per (sequence, q-head): the
 // partition maxima and sums are loaded in parallel (one per thread) into
@@ -904,7 +918,11 @@ template <typename T, int G, bool kFused>
 static pa_status launch_partial(const DecodeParams& prm, int32_t B, int32_t Hkv, int32_t max_parts,
                                 cudaStream_t stream) {
     using Lay = DecodeSmem<kWarps, kStages, G, Row<T>>;
-    auto kern = decode_partition_kernel<T, G, kWarps, kStages, kFused>;
+    void (*kern)(const DecodeParams);
+    if constexpr (Row<T>::kScaled && G <= 4 && !kFused)
+        kern = decode_partition_kernel_4ctas<T, G, kWarps, kStages>;
+    else
+        kern = decode_partition_kernel<T, G, kWarps, kStages, kFused>;
     static bool attr_done[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
