@@ -141,11 +141,16 @@ extern "C" pa_status pa_write_kv(const pa_kv_pool* pool, const void* k_new, cons
         const int64_t rows = (int64_t)num_tokens * pool->num_kv_heads * 2;
         int64_t blocks = (rows * 32 + 255) / 256;
         if (blocks > 1048576) blocks = 1048576;
-        write_kv_fp8_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
+        cudaError_t e = launch_pdl(
+            write_kv_fp8_kernel, dim3((unsigned)blocks), dim3(256), 0, (cudaStream_t)stream,
             (uint8_t*)pool->k_pool, (uint8_t*)pool->v_pool, (float*)pool->k_scale,
             (float*)pool->v_scale, (const uint2*)k_new, (const uint2*)v_new, slot_mapping, rows,
             pool->num_kv_heads, pool->block_size, (int64_t)pool->num_blocks * pool->block_size,
             d_err);
+        if (e != cudaSuccess) {
+            record_cuda_error(e);
+            return PA_ERR_CUDA;
+        }
         return launch_status();
     }
     const int64_t row_bytes = (int64_t)pool->head_dim * dtype_bytes(pool->dtype);
@@ -158,10 +163,17 @@ extern "C" pa_status pa_write_kv(const pa_kv_pool* pool, const void* k_new, cons
     const int threads = 256;
     int64_t blocks = (total + threads - 1) / threads;
     if (blocks > 1048576) blocks = 1048576;
-    write_kv_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
+    // dependent launch: the kernel waits (griddep_wait) for the previous kernel
+    // in the stream before it writes, but its launch overlaps that kernel's tail
+    cudaError_t e = launch_pdl(
+        write_kv_kernel, dim3((unsigned)blocks), dim3(threads), 0, (cudaStream_t)stream,
         (uint4*)pool->k_pool, (uint4*)pool->v_pool, (const uint4*)k_new, (const uint4*)v_new,
         slot_mapping, total, row_vecs, pool->num_kv_heads, pool->block_size,
         (int64_t)pool->num_blocks * pool->block_size, d_err);
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PA_ERR_CUDA;
+    }
     return launch_status();
 }
 
