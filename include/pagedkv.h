@@ -138,6 +138,11 @@ pa_status pa_slot_mapping(const int32_t* table, int32_t n_entries, int32_t block
  * *d_err = PA_ERR_OUT_OF_RANGE.  Two tokens naming the same slot race.
  * Bit-exact copy of the input bits.  num_tokens == 0 enqueues nothing.
  * Requires head_dim * dtype_bytes to be a multiple of 16 (else UNSUPPORTED).
+ * FP8 pools: k_new / v_new are bf16 rows; each (token, kv-head) row is
+ * quantised as the pool description states (codes and its scale written
+ * together; bit-exact against that definition); head_dim must be 128.
+ * The write is a dependent launch: it waits for the previous kernel in the
+ * stream before touching the pool, its launch overlapping that kernel's end.
  */
 pa_status pa_write_kv(const pa_kv_pool* pool, const void* k_new, const void* v_new,
                       const int64_t* slot_mapping, int32_t num_tokens, int32_t* d_err,
@@ -150,8 +155,9 @@ pa_status pa_write_kv(const pa_kv_pool* pool, const void* k_new, const void* v_n
  *   src, dst: device int32[n].
  * An id outside [0, num_blocks) skips that pair and sets *d_err =
  * PA_ERR_OUT_OF_RANGE.  A dst that is also a src or another dst races.
- * Bit-exact.  n == 0 enqueues nothing.  Enqueue it before the write that
- * follows the copy-on-write decision, on the same stream.
+ * Bit-exact; for FP8 pools the blocks' row scales are copied with the codes.
+ * n == 0 enqueues nothing.  Enqueue it before the write that follows the
+ * copy-on-write decision, on the same stream.
  */
 pa_status pa_copy_blocks(const pa_kv_pool* pool, const int32_t* src, const int32_t* dst,
                          int32_t n, int32_t* d_err, pa_stream_t stream);
@@ -194,9 +200,10 @@ pa_status pa_decode_workspace_bytes(const pa_kv_pool* pool, int32_t num_seqs,
  *   out:          device float32 [num_seqs][num_q_heads][head_dim].
  *   workspace:    device, >= pa_decode_workspace_bytes(...) bytes, 16-byte
  *                 aligned; may be NULL when that size is 0.
- * Implemented: head_dim * dtype_bytes == 256 (bf16 D=128, f32 D=64), block
- * size a power of two, num_q_heads / num_kv_heads in {1, 2, 4, 8}; other
- * valid shapes return UNSUPPORTED.  A table entry outside the pool skips its
+ * Implemented: head_dim * dtype_bytes == 256 (bf16 D=128, f32 D=64) or FP8
+ * pages with D=128 and block size >= 4 (q is then bf16), block size a power of
+ * two, num_q_heads / num_kv_heads in {1, 2, 4, 8}; other valid shapes return
+ * UNSUPPORTED.  A table entry outside the pool skips its
  * tokens and sets *d_err.
  */
 pa_status pa_decode(const pa_kv_pool* pool, const void* q, int32_t num_q_heads,

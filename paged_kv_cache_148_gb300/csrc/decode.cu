@@ -31,6 +31,12 @@
 //  * The CTA's warps combine in shared memory; a single-partition sequence
 //    writes the normalised output directly, otherwise (m, l, acc) partials go
 //    to the workspace and decode_merge_kernel finishes.
+//  * FP8 pages (Row<uint8_t>): 128-byte code rows, 8-byte lane columns, and
+//    each chunk's 16 K and 16 V row scales in the same ring stage; the K
+//    scale multiplies the finished score, the V scale is folded into the
+//    probability pair (the running sum keeps the plain probability).
+//  * Sliding window (pa_decode_window): partitions start at the window's
+//    first chunk and rows before it are masked.
 //  * Fused step (pa_decode_step): the same kernel also writes the new token
 //    of (sequence, kv-head) into its slot, and into the shared-memory copy of
 //    the chunk that holds it (P1 §4.1), and the last partition CTA of each

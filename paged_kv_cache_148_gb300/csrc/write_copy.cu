@@ -5,7 +5,10 @@
 //
 // Both are pure HBM copies.  Each thread moves 16-byte vectors, consecutive
 // threads touch consecutive vectors of one row or page, so every warp access
-// is a fully used 512-byte span on both the read and the write side.
+// is a fully used 512-byte span on both the read and the write side.  FP8
+// pages are written by a separate kernel that quantises each bf16 row (one
+// warp per row) and stores its codes and scale; the copy moves the scales
+// along with the code pages.
 #include "common.cuh"
 #include "host_common.h"
 
