@@ -224,3 +224,34 @@ def test_workspace_sizes(L):
     pt = ctypes.c_int32()
     assert L.pa_decode_partition_tokens(pp, 64, 32, 4097, ctypes.byref(pt)) == 0
     assert pt.value > 0 and pt.value % 16 == 0
+
+
+def test_fp8_pool_page_size_and_argument_checks(L):
+    # FP8 pages count one byte per element plus a float32 scale per row
+    pool = pkv.pa_kv_pool(1, 1, 10, 16, 2, 128, pkv.DTYPE_FP8_E4M3, 16, 16)
+    out = ctypes.c_int64()
+    assert L.pa_page_size_bytes(ctypes.byref(pool), ctypes.byref(out)) == 0
+    assert out.value == 2 * 16 * 2 * (128 + 4)
+    P = ctypes.c_void_p
+    pp = ctypes.byref(pool)
+    # the scale arrays are required
+    nos = pkv.pa_kv_pool(16, 16, 10, 16, 2, 128, pkv.DTYPE_FP8_E4M3, None, None)
+    assert L.pa_write_kv(ctypes.byref(nos), P(16), P(16), P(16), 1, None, None) == \
+        pkv.PA_ERR_INVALID_ARG
+    # only D = 128 rows are written; decode needs blocks of at least 4 tokens
+    pool.head_dim = 64
+    assert L.pa_write_kv(pp, P(16), P(16), P(16), 1, None, None) == pkv.PA_ERR_UNSUPPORTED
+    pool.head_dim = 128
+    pool.block_size = 2
+    args = [P(16), 4, P(16), 4, P(16), 2, 64, ctypes.c_float(0.1), 0, P(16), None, 0, None, None]
+    assert L.pa_decode(pp, *args) == pkv.PA_ERR_UNSUPPORTED
+    # the one-launch step writes raw rows and so takes no FP8 pool
+    pool.block_size = 16
+    step = [P(16), P(16), P(16), P(16), 4, P(16), 4, P(16), 2, 64, ctypes.c_float(0.1), 0,
+            P(16), None, 0, None, None]
+    assert L.pa_decode_step(pp, *step) == pkv.PA_ERR_UNSUPPORTED
+    # a window must be positive
+    win = [P(16), 4, P(16), 4, P(16), 2, 64, 0, ctypes.c_float(0.1), 0, P(16), None, 0, None,
+           None]
+    pool.dtype = pkv.DTYPE_BF16
+    assert L.pa_decode_window(pp, *win) == pkv.PA_ERR_INVALID_ARG
