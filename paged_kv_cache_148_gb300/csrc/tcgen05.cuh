@@ -1,7 +1,7 @@
 // Blackwell (sm_100 family) tensor-core and TMA wrappers as inline PTX:
-// TMEM allocation, tcgen05.mma (kind::f16, one CTA), commit to an mbarrier,
-// TMEM <-> register moves, shared-memory matrix descriptors and tiled TMA
-// loads through a CUtensorMap.
+// TMEM allocation, tcgen05.mma (kind::f16, one CTA, issued by an elected lane
+// of a converged warp), commit to an mbarrier, TMEM loads, shared-memory
+// matrix descriptors and tiled TMA loads through a CUtensorMap.
 #pragma once
 
 #include <cstdint>
@@ -67,25 +67,6 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int
 }
 
 // ----------------------------------------------------------------- MMA
-// D[tmem] (+)= A[smem desc] * B[smem desc] (kind::f16: bf16 or fp16 operands,
-// per the instruction descriptor); issued by one thread.
-PA_DEVICE void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                        uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
-}
-
-// Arrive on `bar` once every tcgen05 operation issued so far by this thread
-// has completed.
-PA_DEVICE void commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-        ::"r"(smem_u32(bar)) : "memory");
-}
-
 // Warp-collective issue: every lane of a converged warp makes the call and
 // elect.sync picks the lane that issues the instruction (the same lane each
 // time, so the in-order and commit rules for one issuing thread hold).  With
@@ -112,7 +93,8 @@ PA_DEVICE void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, ui
         ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
-// commit() by the elected lane of a converged warp.
+// Arrive on `bar` once every tcgen05 operation issued so far by the elected
+// lane (the issuing thread) has completed.
 PA_DEVICE void commit_warp(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
@@ -135,18 +117,6 @@ PA_DEVICE void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
         : "r"(taddr));
-}
-PA_DEVICE void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
-          "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
-          "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]),
-          "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
-          "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
 }
 PA_DEVICE void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 PA_DEVICE void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
