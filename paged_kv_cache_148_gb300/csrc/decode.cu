@@ -874,8 +874,16 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
 // ---------------------------------------------------------------- host side
 constexpr int kWarps = 4;
 constexpr int kStages = 2;
-constexpr int kCtasPerSm = 3;
 constexpr int kWaves = 9;
+
+// Partition CTAs per SM the plan counts on: 3 (the shared-memory limit of
+// 16-bit and f32 rows), 2 at G = 8, where registers allow only two.  (FP8 rows
+// at G <= 4 run 4 per SM, but measured fastest with the 3-per-SM plan: more
+// partitions cost more in the merge than they gain in balance.)
+static int ctas_per_sm(const pa_kv_pool* pool, int32_t Hq) {
+    const int G = pool->num_kv_heads > 0 ? Hq / pool->num_kv_heads : 1;
+    return G >= 8 ? 2 : 3;
+}
 
 struct Plan {
     int32_t part_chunks;
@@ -898,7 +906,7 @@ static pa_status make_plan(const pa_kv_pool* pool, int32_t B, int32_t Hq, int32_
         pc = partition_tokens / kChunk;
     } else if (partition_tokens == 0) {
         const int64_t units = (int64_t)B * pool->num_kv_heads;
-        const int64_t target = (int64_t)device_sm_count() * kCtasPerSm * kWaves;
+        const int64_t target = (int64_t)device_sm_count() * ctas_per_sm(pool, Hq) * kWaves;
         pc = (units * chunks_max + target - 1) / (target > 0 ? target : 1);
         if (pc < 2 * kWarps) pc = 2 * kWarps;
         pc = (pc + kWarps - 1) / kWarps * kWarps;
