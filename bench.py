@@ -94,6 +94,23 @@ def algorithmic_bytes(wl, window: int = 0) -> dict:
             "decode_total": kv + q + out + tables + lens}
 
 
+def physical_kv_bytes(wl, tables, window: int = 0) -> int:
+    """K/V bytes of the distinct physical pages one decode step reads.  A page
+    that several sequences reference (a forked prefix) counts once, with the
+    union of the rows they read from it; the logical count in
+    algorithmic_bytes counts it once per sequence."""
+    bp = wl.block_size
+    rows = {}
+    for s, table in enumerate(tables):
+        n = int(wl.total_lens[s])
+        lo = max(n - window, 0) if window > 0 else 0
+        for j in range(lo // bp, -(-n // bp)):
+            a, b = max(j * bp, lo) - j * bp, min((j + 1) * bp, n) - j * bp
+            blk = int(table[j])
+            rows[blk] = rows.get(blk, 0) | (((1 << (b - a)) - 1) << a)
+    return sum(bin(m).count("1") for m in rows.values()) * wl.logical_bytes_per_token()
+
+
 def ab_kv_mb(wl, window: int = 0) -> float:
     return algorithmic_bytes(wl, window)["kv"] / 1e6
 
@@ -426,6 +443,9 @@ def run_ours(args, rank, world, local_rank):
                     "pa_write_kv + pa_prefill"),
            "partition_tokens": args.partition_tokens or "auto"}
     if is_decode:
+        cfg["kv_bytes"] = {"logical": ab["kv"],
+                           "unique_physical": physical_kv_bytes(wl, g.tables_list(), window),
+                           "counted": "logical (each sequence's pages once per sequence)"}
         per_rank = ab["decode_total"]
         res.update({"value": aggregate_value(per_rank, world, ms), "unit": "GB/s",
                     "higher_is_better": True,

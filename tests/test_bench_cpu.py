@@ -78,6 +78,44 @@ def test_algorithmic_bytes_with_a_window():
     assert ab["q"] == full["q"] and ab["out"] == full["out"]
 
 
+def _distinct_rows(wl, tables, window=0):
+    # set of (physical block, offset) pairs any sequence reads
+    seen = set()
+    for s, table in enumerate(tables):
+        n = int(wl.total_lens[s])
+        lo = max(n - window, 0) if window else 0
+        seen |= {(table[i // wl.block_size], i % wl.block_size) for i in range(lo, n)}
+    return len(seen)
+
+
+def test_physical_bytes_equal_logical_without_sharing():
+    import oracle
+    wl = workloads.decode_gqa(scale=1 / 16)
+    tables = oracle.OracleCache(wl).tables
+    assert bench.physical_kv_bytes(wl, tables) == bench.algorithmic_bytes(wl)["kv"]
+    assert bench.physical_kv_bytes(wl, tables, 50) == bench.algorithmic_bytes(wl, 50)["kv"]
+
+
+def test_physical_bytes_count_a_shared_prefix_once():
+    import oracle
+    wl = workloads.decode_long_shared(scale=1 / 256)
+    tables = oracle.OracleCache(wl).tables
+    per_token = 2 * wl.num_kv_heads * wl.head_dim * 2
+    phys = bench.physical_kv_bytes(wl, tables)
+    assert phys == _distinct_rows(wl, tables) * per_token
+    # logical - physical = the rows of every pair's fully shared pages (the
+    # partly filled shared page is copied on write, so it is not shared)
+    shared = 0
+    for s in range(wl.num_seqs):
+        p = int(wl.pair_of[s])
+        if p > s:
+            shared += int(wl.prefix_len[s]) // wl.block_size * wl.block_size
+    assert shared > 0
+    assert bench.algorithmic_bytes(wl)["kv"] - phys == shared * per_token
+    w = 200
+    assert bench.physical_kv_bytes(wl, tables, w) == _distinct_rows(wl, tables, w) * per_token
+
+
 def test_prefill_flops_matches_closed_form():
     wl = workloads.prefill()
     # 16 sequences, queries at positions 2048..2559 see pos+1 keys
