@@ -196,7 +196,9 @@ pa_status pa_decode_workspace_bytes(const pa_kv_pool* pool, int32_t num_seqs,
  *                 ceil(n / B_p) are never read.
  *   context_lens: device int32 [num_seqs], tokens to attend to including the
  *                 new one (1 <= n <= max_context; 0 leaves out[s] untouched).
- *   max_context:  host upper bound of context_lens (sizes the plan).
+ *   max_context:  host upper bound of context_lens (sizes the plan); a
+ *                 longer context is cut to its first max_context positions
+ *                 and sets *d_err = PA_ERR_OUT_OF_RANGE.
  *   out:          device float32 [num_seqs][num_q_heads][head_dim].
  *   workspace:    device, >= pa_decode_workspace_bytes(...) bytes, 16-byte
  *                 aligned; may be NULL when that size is 0.
@@ -326,7 +328,8 @@ pa_status pa_decode_step(const pa_kv_pool* pool, const void* k_new, const void* 
  *   context_lens: device int32 [num_seqs].
  *   block_tables: device int32 [num_seqs][max_blocks_per_seq].
  *   max_q_len:    host upper bound of the per-sequence query counts (grid).
- *   max_context:  host upper bound of context_lens.
+ *   max_context:  host upper bound of context_lens (checked >= 0; the grid
+ *                 depends only on max_q_len, so the kernel does not use it).
  *   out:          device float32 [total_q][num_q_heads][head_dim].
  * Implemented: bf16, head_dim 128, block size a power of two in [8, 128],
  * num_q_heads / num_kv_heads in {1, 2, 4, 8}, pool and q 16-byte aligned.

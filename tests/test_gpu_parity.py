@@ -221,6 +221,25 @@ def test_decode_flags_table_entry_outside_pool():
     assert int(g.err.item()) in (pkv.PA_ERR_OUT_OF_RANGE, pkv.PA_ERR_NEGATIVE_BLOCK)
 
 
+def test_decode_clamps_contexts_above_max_context():
+    # a context longer than max_context is cut to its first max_context
+    # positions and flagged; the other sequences are unaffected
+    wl = workloads.decode_gqa(scale=1 / 8)
+    g = GpuWorkload(wl)
+    g.write_new()
+    n = wl.total_lens.astype(np.int64)
+    cap = int(n.max()) - 5
+    assert cap >= 1 and int((n > cap).sum()) >= 1
+    g.err.zero_()
+    out = pkv.decode(g.cache.pool, g.q, g.block_tables, g.context_lens, cap, wl.scale, d_err=g.err)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == pkv.PA_ERR_OUT_OF_RANGE
+    oc = oracle.OracleCache(wl)
+    ref = oracle.decode(oc.k, oc.v, oracle.to_numpy_bits(g.q_host), oc.tables,
+                        np.minimum(n, cap), wl.scale)
+    assert_close(out.cpu().numpy(), ref, "bf16", "max_context=%d" % cap)
+
+
 # ---------------------------------------------------------------- full-size workloads
 @pytest.mark.parametrize("make", [workloads.decode_tiny, workloads.decode_gqa,
                                   workloads.decode_mha, workloads.decode_long_shared],
