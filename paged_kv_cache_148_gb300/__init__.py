@@ -155,6 +155,43 @@ def _need(t: torch.Tensor, name: str, dtype=None, device=None):
         raise ValueError("%s must be contiguous" % name)
 
 
+def _need_shape(t: torch.Tensor, name: str, shape):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def _need_err(d_err: Optional[torch.Tensor], device):
+    """The device error word: None, or an int32 tensor on the pool's device."""
+    if d_err is not None:
+        _need(d_err, "d_err", torch.int32, device)
+        if d_err.numel() < 1:
+            raise ValueError("d_err must hold at least one int32")
+
+
+def _need_workspace(ws: Optional[torch.Tensor], device):
+    if ws is not None:
+        _need(ws, "workspace", None, device)
+
+
+def _need_decode_args(pool, q, block_tables, context_lens, out):
+    """Shapes of a decode call: q [B][H_q][D], block_tables [B][max_blocks],
+    context_lens [B], out [B][H_q][D] float32 (when given)."""
+    _need(q, "q", pool.io_dtype, pool.device)
+    _need(block_tables, "block_tables", torch.int32, pool.device)
+    _need(context_lens, "context_lens", torch.int32, pool.device)
+    if q.dim() != 3 or q.shape[2] != pool.head_dim:
+        raise ValueError("q must be [B][H_q][%d], got %s" % (pool.head_dim, tuple(q.shape)))
+    B, Hq, D = q.shape
+    if block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be [%d][max_blocks], got %s"
+                         % (B, tuple(block_tables.shape)))
+    _need_shape(context_lens, "context_lens", (B,))
+    if out is not None:
+        _need(out, "out", torch.float32, pool.device)
+        _need_shape(out, "out", (B, Hq, D))
+    return B, Hq, D
+
+
 # --------------------------------------------------------------------------- pool
 class KVPool:
     """K and V block pools [num_blocks][num_kv_heads][block_size][head_dim] on one device.
@@ -243,6 +280,8 @@ def write_kv(pool: KVPool, k_new: torch.Tensor, v_new: torch.Tensor, slot_mappin
     _need(slot_mapping, "slot_mapping", torch.int64, pool.device)
     if tuple(k_new.shape) != (T, pool.num_kv_heads, pool.head_dim) or k_new.shape != v_new.shape:
         raise ValueError("k_new/v_new must be [T][H_kv][D] with T = len(slot_mapping)")
+    _need_shape(slot_mapping, "slot_mapping", (T,))
+    _need_err(d_err, pool.device)
     _check(lib().pa_write_kv(pool.c, _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T,
                              _ptr(d_err), _stream(stream)), "pa_write_kv")
 
@@ -254,6 +293,7 @@ def copy_blocks(pool: KVPool, src: torch.Tensor, dst: torch.Tensor,
     _need(dst, "dst", torch.int32, pool.device)
     if src.shape != dst.shape or src.dim() != 1:
         raise ValueError("src and dst must be 1-D of equal length")
+    _need_err(d_err, pool.device)
     _check(lib().pa_copy_blocks(pool.c, _ptr(src), _ptr(dst), int(src.shape[0]), _ptr(d_err),
                                 _stream(stream)), "pa_copy_blocks")
 
@@ -283,13 +323,13 @@ def decode(pool: KVPool, q: torch.Tensor, block_tables: torch.Tensor, context_le
     phase: "all" (pa_decode), "partial" (pa_decode_partial) or "merge"
     (pa_decode_merge, which needs the workspace the partial phase filled).
     """
-    _need(q, "q", pool.io_dtype, pool.device)
-    _need(block_tables, "block_tables", torch.int32, pool.device)
-    _need(context_lens, "context_lens", torch.int32, pool.device)
-    B, Hq, D = q.shape
+    B, Hq, D = _need_decode_args(pool, q, block_tables, context_lens, out)
+    _need_workspace(workspace, pool.device)
+    _need_err(d_err, pool.device)
+    if phase not in ("all", "partial", "merge"):
+        raise ValueError("phase must be 'all', 'partial' or 'merge'")
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=pool.device)
-    _need(out, "out", torch.float32, pool.device)
     need = decode_workspace_bytes(pool, B, Hq, max_context, partition_tokens)
     if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=pool.device)
@@ -324,13 +364,11 @@ def decode_window(pool: KVPool, q: torch.Tensor, block_tables: torch.Tensor,
                   stream=None) -> torch.Tensor:
     """Sliding-window paged decode: the query at position n-1 attends to the last
     `window` positions; returns out [B][H_q][D] float32."""
-    _need(q, "q", pool.io_dtype, pool.device)
-    _need(block_tables, "block_tables", torch.int32, pool.device)
-    _need(context_lens, "context_lens", torch.int32, pool.device)
-    B, Hq, D = q.shape
+    B, Hq, D = _need_decode_args(pool, q, block_tables, context_lens, out)
+    _need_workspace(workspace, pool.device)
+    _need_err(d_err, pool.device)
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=pool.device)
-    _need(out, "out", torch.float32, pool.device)
     need = decode_window_workspace_bytes(pool, B, Hq, max_context, window, partition_tokens)
     if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=pool.device)
@@ -371,17 +409,15 @@ def decode_step(pool: KVPool, k_new: torch.Tensor, v_new: torch.Tensor, slot_map
     _need(k_new, "k_new", pool.io_dtype, pool.device)
     _need(v_new, "v_new", pool.io_dtype, pool.device)
     _need(slot_mapping, "slot_mapping", torch.int64, pool.device)
-    _need(q, "q", pool.io_dtype, pool.device)
-    _need(block_tables, "block_tables", torch.int32, pool.device)
-    _need(context_lens, "context_lens", torch.int32, pool.device)
-    B, Hq, D = q.shape
+    B, Hq, D = _need_decode_args(pool, q, block_tables, context_lens, out)
     if tuple(k_new.shape) != (B, pool.num_kv_heads, pool.head_dim) or k_new.shape != v_new.shape:
         raise ValueError("k_new/v_new must be [B][H_kv][D]")
     if tuple(slot_mapping.shape) != (B,):
         raise ValueError("slot_mapping must be [B]")
+    _need_workspace(workspace, pool.device)
+    _need_err(d_err, pool.device)
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=pool.device)
-    _need(out, "out", torch.float32, pool.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().pa_decode_step(pool.c, _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(q), Hq,
                                 _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
@@ -400,10 +436,21 @@ def prefill(pool: KVPool, q: torch.Tensor, cu_seqlens_q: torch.Tensor, context_l
     _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, pool.device)
     _need(context_lens, "context_lens", torch.int32, pool.device)
     _need(block_tables, "block_tables", torch.int32, pool.device)
+    if q.dim() != 3 or q.shape[2] != pool.head_dim:
+        raise ValueError("q must be [T][H_q][%d], got %s" % (pool.head_dim, tuple(q.shape)))
     T, Hq, D = q.shape
+    B = int(context_lens.shape[0]) if context_lens.dim() == 1 else -1
+    if B < 0:
+        raise ValueError("context_lens must be 1-D")
+    _need_shape(cu_seqlens_q, "cu_seqlens_q", (B + 1,))
+    if block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be [%d][max_blocks], got %s"
+                         % (B, tuple(block_tables.shape)))
+    _need_err(d_err, pool.device)
     if out is None:
         out = torch.empty((T, Hq, D), dtype=torch.float32, device=pool.device)
     _need(out, "out", torch.float32, pool.device)
+    _need_shape(out, "out", (T, Hq, D))
     _check(lib().pa_prefill(pool.c, _ptr(q), T, Hq, _ptr(cu_seqlens_q), _ptr(context_lens),
                             _ptr(block_tables), int(block_tables.shape[1]),
                             int(context_lens.shape[0]), int(max_q_len), int(max_context),
