@@ -255,3 +255,34 @@ def test_fp8_pool_page_size_and_argument_checks(L):
            None]
     pool.dtype = pkv.DTYPE_BF16
     assert L.pa_decode_window(pp, *win) == pkv.PA_ERR_INVALID_ARG
+
+
+def test_plan_properties_over_random_shapes(L):
+    # the automatic partition size is a whole number of 4-warp rounds of
+    # 16-token chunks, and every workspace holds (max, sum, D values) for each
+    # (sequence, q-head, partition); a window never needs more than the whole
+    # context
+    rng = np.random.default_rng(23)
+    for _ in range(300):
+        Hkv = int(rng.choice([1, 2, 4, 8, 16]))
+        G = int(rng.choice([1, 2, 4, 8]))
+        B = int(rng.integers(1, 300))
+        max_ctx = int(rng.integers(1, 300000))
+        pool = pkv.pa_kv_pool(16, 16, 1000, 16, Hkv, 128, pkv.DTYPE_BF16)
+        pp = ctypes.byref(pool)
+        pt = ctypes.c_int32()
+        assert L.pa_decode_partition_tokens(pp, B, G * Hkv, max_ctx, ctypes.byref(pt)) == 0
+        assert pt.value >= 128 and pt.value % 64 == 0
+        out = ctypes.c_size_t()
+        assert L.pa_decode_workspace_bytes(pp, B, G * Hkv, max_ctx, 0, ctypes.byref(out)) == 0
+        parts = -(-(-(-max_ctx // 16)) // (pt.value // 16))
+        if parts > 1:
+            assert out.value >= B * G * Hkv * parts * (128 + 2) * 4
+        else:
+            assert out.value == 0
+        w = int(rng.integers(1, 5000))
+        wout = ctypes.c_size_t()
+        assert L.pa_decode_window_workspace_bytes(pp, B, G * Hkv, max_ctx, w, 0,
+                                                  ctypes.byref(wout)) == 0
+        if w >= max_ctx:
+            assert wout.value <= out.value
