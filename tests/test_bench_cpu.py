@@ -135,3 +135,17 @@ def test_reference_arm_prints_contract_line():
         assert k in line
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_recorded_traffic_is_dropped_when_the_sources_change(monkeypatch):
+    import json as _json
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rec = _json.load(f)["decode_partition_kernel"]["decode_gqa"]
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda k: rec["source_hash"])
+    assert bench.recorded_traffic("decode_partition_kernel", "decode_gqa") == \
+        rec["dram_bytes_per_launch"]
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda k: "0" * 16)
+    assert bench.recorded_traffic("decode_partition_kernel", "decode_gqa") is None
+    assert bench.recorded_traffic("decode_partition_kernel", "no_such_workload") is None
+    # a recorded figure is DRAM read + write of one launch
+    assert rec["dram_bytes_per_launch"] == rec["dram_read"] + rec["dram_write"]
