@@ -15,7 +15,9 @@
  * Conventions for every entry point:
  *  - Ownership: the caller owns every buffer.  Device pointers must stay valid
  *    until the work enqueued on `stream` has finished.  Nothing here allocates
- *    device memory; scratch space is passed in (pa_decode's workspace).
+ *    device memory at run time; scratch space is passed in (pa_decode's
+ *    workspace), except for pa_decode_noalloc, whose scratch is a 16 MiB
+ *    static array in the library's device image.
  *  - Asynchrony: device entry points only enqueue kernels on `stream` (NULL =
  *    the legacy default stream) and return; there is no internal sync.
  *    Ordering between calls (copy-on-write copy before the write that follows
@@ -207,6 +209,11 @@ pa_status pa_decode_workspace_bytes(const pa_kv_pool* pool, int32_t num_seqs,
  * two, num_q_heads / num_kv_heads in {1, 2, 4, 8}; other valid shapes return
  * UNSUPPORTED.  A table entry outside the pool skips its
  * tokens and sets *d_err.
+ * Arithmetic: bf16 pools with D = 128, pages of >= 16 tokens and 2, 4 or 8
+ * q-heads per kv-head run the score and P V products on tensor cores
+ * (bf16 operands, float32 accumulation; the probabilities enter P V as a
+ * bf16 high part plus a bf16 low part, about 16 significant bits); all other
+ * shapes run them in float32 on CUDA cores.
  */
 pa_status pa_decode(const pa_kv_pool* pool, const void* q, int32_t num_q_heads,
                     const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -236,18 +243,24 @@ pa_status pa_decode_merge(const pa_kv_pool* pool, int32_t num_q_heads,
 
 /*
  * pa_decode without a caller-provided workspace, for callers that cannot
- * allocate device memory when they run decode: code being recorded into a
- * CUDA graph (no cudaMalloc while a capture is open), plugin hosts that pass
- * raw pointers but no allocator, and processes whose HBM is all given to the
- * block pool.  The pages have no counterpart to this entry point.
- * Same arguments and results as pa_decode minus workspace/workspace_bytes.
- * The split-KV partials live in a static device array of 16 MiB that the
- * library's device image carries (every GPU that loads the library holds it
- * until the process exits).  A shape whose pa_decode_workspace_bytes exceeds
- * 16 MiB returns PA_ERR_UNSUPPORTED and enqueues nothing.  Allocates nothing.
- * The first call on each device (with that device current) looks up the
- * array's address; make it before any stream capture.  All calls share the
- * array: calls that may overlap on the GPU (unordered streams) race.
+ * allocate device memory when they run decode: plugin or custom-op hosts that
+ * hand over raw device pointers but no allocator, and serving processes that
+ * give all spare HBM to the block pool and keep no allocator headroom.  The
+ * pages have no counterpart to this entry point.
+ * Same arguments, kernels, partition plan and results as pa_decode minus
+ * workspace/workspace_bytes.  The split-KV partials live in a static device
+ * array of 16 MiB that the library's device image carries (every GPU that
+ * loads the library's kernels holds it until the process exits).  A shape
+ * whose pa_decode_workspace_bytes exceeds 16 MiB returns PA_ERR_UNSUPPORTED
+ * and enqueues nothing.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ * Set-up: the first call in each CUDA context (the device's context, current
+ * on the calling thread) looks up the array's address and caches it under
+ * the context's unique id (a context created again after cudaDeviceReset is
+ * looked up afresh); make the first call on each device before any stream
+ * capture.  All calls share the array: calls that may overlap on the GPU
+ * (unordered streams) race.  After *d_err = PA_ERR_TIMEOUT the output may
+ * hold partials of an earlier call and must be discarded.
  */
 pa_status pa_decode_noalloc(const pa_kv_pool* pool, const void* q, int32_t num_q_heads,
                             const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -275,6 +288,41 @@ pa_status pa_decode_window(const pa_kv_pool* pool, const void* q, int32_t num_q_
                            int32_t window, float scale, int32_t partition_tokens, float* out,
                            void* workspace, size_t workspace_bytes, int32_t* d_err,
                            pa_stream_t stream);
+
+/*
+ * Shared-prefix-aware decode ("03｜PagedAttention 与 KV Cache 内存系统" §5:
+ * sequences forked from one prefix hold the same physical blocks, and only a
+ * partially filled shared tail is copied before a write; "PagedAttention 的原
+ * 理是什么？…" §四: two requests with a common prefix point at the same
+ * physical block, refcount 2).  Same result as pa_decode (the same float32
+ * definition for every sequence), but a declared pair's shared pages are
+ * read from HBM once for both members: one unit of work scores each shared
+ * page against the q-heads of both sequences.
+ *   partner:      device int32 [num_seqs]: the other member of s's pair, or -1.
+ *   shared_lens:  device int32 [num_seqs]: tokens on the pair's shared
+ *                 leading pages (the tables of both members hold the same
+ *                 ids for the first shared_lens / block_size entries).
+ * A declaration is used only if it is mutual (partner[partner[s]] == s, equal
+ * shared_lens on both sides), shared_lens is a positive multiple of the block
+ * size and of 16, and no longer than either member's context; otherwise
+ * *d_err = PA_ERR_INVALID_ARG and both members are decoded on their own
+ * (still correct).  Tables that differ over declared shared pages set
+ * *d_err = PA_ERR_INVALID_ARG and leave that pair's outputs undefined.
+ * Implemented: bf16 pools, head_dim 128, power-of-two block size >= 16,
+ * num_q_heads / num_kv_heads in {1, 2, 4, 8}; no sliding window.  The
+ * workspace (pa_decode_shared_workspace_bytes, one partition slot per
+ * sequence more than pa_decode's) holds the partials.  Other arguments,
+ * limits and errors as pa_decode.
+ */
+pa_status pa_decode_shared_workspace_bytes(const pa_kv_pool* pool, int32_t num_seqs,
+                                           int32_t num_q_heads, int32_t max_context,
+                                           int32_t partition_tokens, size_t* bytes);
+pa_status pa_decode_shared(const pa_kv_pool* pool, const void* q, int32_t num_q_heads,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, int32_t num_seqs, int32_t max_context,
+                           const int32_t* partner, const int32_t* shared_lens, float scale,
+                           int32_t partition_tokens, float* out, void* workspace,
+                           size_t workspace_bytes, int32_t* d_err, pa_stream_t stream);
 
 /*
  * One decode step in a single launch: the fused form of pa_write_kv of one
@@ -335,6 +383,14 @@ pa_status pa_decode_step(const pa_kv_pool* pool, const void* k_new, const void* 
  * num_q_heads / num_kv_heads in {1, 2, 4, 8}, pool and q 16-byte aligned.
  * A table entry outside the pool is read as block 0 and sets *d_err; a
  * sequence with context_lens < its query count sets PA_ERR_INVALID_ARG.
+ * Precision: Q K^T runs on the bf16 operands; P V runs on fp16 operands (the
+ * probabilities and the V values rounded to fp16, to nearest even), both
+ * with float32 accumulation.  So the V values must lie within the fp16
+ * range: |v| <= 65504 is exact apart from magnitudes below 2^-14, which are
+ * fp16 subnormals (absolute rounding error <= 2^-25).  A V value of
+ * magnitude >= 65536 (the next bf16 above 65504) or an infinity is
+ * saturated to +-65504 and sets *d_err = PA_ERR_UNSUPPORTED; the output is
+ * then the attention over the saturated values.
  */
 pa_status pa_prefill(const pa_kv_pool* pool, const void* q, int32_t total_q,
                      int32_t num_q_heads, const int32_t* cu_seqlens_q,

@@ -42,7 +42,8 @@ EXPORTED = [
     "pa_physical_slot", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks",
     "pa_decode_partition_tokens", "pa_decode_workspace_bytes", "pa_decode", "pa_decode_partial",
     "pa_decode_merge", "pa_decode_noalloc", "pa_decode_step_workspace_bytes", "pa_decode_step",
-    "pa_decode_window_workspace_bytes", "pa_decode_window",
+    "pa_decode_window_workspace_bytes", "pa_decode_window", "pa_decode_shared_workspace_bytes",
+    "pa_decode_shared",
     "pa_prefill",
     "pa_alloc_create", "pa_alloc_destroy", "pa_alloc_append", "pa_alloc_fork",
     "pa_alloc_writable_tail", "pa_alloc_reserve", "pa_alloc_release", "pa_alloc_refcount",
@@ -103,6 +104,8 @@ def lib() -> ctypes.CDLL:
         "pa_decode_window_workspace_bytes": ([P, i32, i32, i32, i32, i32, P], i32),
         "pa_decode_window": ([P, P, i32, P, i32, P, i32, i32, i32, f32, i32, P, P, sz, P, P], i32),
         "pa_decode_step": ([P, P, P, P, P, i32, P, i32, P, i32, i32, f32, i32, P, P, sz, P, P], i32),
+        "pa_decode_shared_workspace_bytes": ([P, i32, i32, i32, i32, P], i32),
+        "pa_decode_shared": ([P, P, i32, P, i32, P, i32, i32, P, P, f32, i32, P, P, sz, P, P], i32),
         "pa_prefill": ([P, P, i32, i32, P, P, P, i32, i32, i32, i32, f32, i32, P, P, P], i32),
         "pa_alloc_create": ([i32, P, P], i32),
         "pa_alloc_destroy": ([P], None),
@@ -344,6 +347,47 @@ def decode(pool: KVPool, q: torch.Tensor, block_tables: torch.Tensor, context_le
               _ptr(context_lens), B, int(max_context), float(scale), int(partition_tokens),
               _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_err), _stream(stream)),
            "pa_decode" if phase == "all" else "pa_decode_partial")
+    return out
+
+
+def decode_shared_workspace_bytes(pool: KVPool, num_seqs: int, num_q_heads: int,
+                                  max_context: int, partition_tokens: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().pa_decode_shared_workspace_bytes(pool.c, num_seqs, num_q_heads, max_context,
+                                                  partition_tokens, ctypes.byref(out)),
+           "pa_decode_shared_workspace_bytes")
+    return out.value
+
+
+def decode_shared(pool: KVPool, q: torch.Tensor, block_tables: torch.Tensor,
+                  context_lens: torch.Tensor, max_context: int, partner: torch.Tensor,
+                  shared_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
+                  workspace: Optional[torch.Tensor] = None, partition_tokens: int = 0,
+                  d_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Shared-prefix-aware paged decode (pa_decode_shared); returns out [B][H_q][D].
+
+    partner: int32 [B] (the other member of a pair, or -1); shared_lens: int32
+    [B], tokens on the pair's shared leading pages.
+    """
+    B, Hq, D = _need_decode_args(pool, q, block_tables, context_lens, out)
+    _need(partner, "partner", torch.int32, pool.device)
+    _need(shared_lens, "shared_lens", torch.int32, pool.device)
+    _need_shape(partner, "partner", (B,))
+    _need_shape(shared_lens, "shared_lens", (B,))
+    _need_workspace(workspace, pool.device)
+    _need_err(d_err, pool.device)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=pool.device)
+    need = decode_shared_workspace_bytes(pool, B, Hq, max_context, partition_tokens)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=pool.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode_shared(pool.c, _ptr(q), Hq, _ptr(block_tables),
+                                  int(block_tables.shape[1]), _ptr(context_lens), B,
+                                  int(max_context), _ptr(partner), _ptr(shared_lens),
+                                  float(scale), int(partition_tokens), _ptr(out),
+                                  _ptr(workspace), ws_bytes, _ptr(d_err), _stream(stream)),
+           "pa_decode_shared")
     return out
 
 

@@ -49,6 +49,7 @@
 
 #include "common.cuh"
 #include "host_common.h"
+#include "tcgen05.cuh"
 
 namespace pa {
 
@@ -86,6 +87,10 @@ struct DecodeParams {
     // FP8 pages: float row scales [num_blocks][H_kv][B_p]
     const float* k_scale;
     const float* v_scale;
+    // shared-prefix decode only: declared pairs (nullptr otherwise)
+    const int32_t* partner;       // [B] the other member of a pair, or -1
+    const int32_t* shared_lens;   // [B] tokens on the pair's shared leading pages
+    int32_t num_seqs;
 };
 
 // Storage types of a pool row.  A lane owns one column of kColBytes bytes of a
@@ -771,6 +776,10 @@ __global__ void __launch_bounds__(W * 32, 4) decode_partition_kernel_4ctas(const
     decode_partition_body<T, G, W, S, false>(p);
 }
 
+}  // namespace pa
+#include "decode_mma.cuh"
+namespace pa {
+
 // Merge of split-KV partials (P1 §4): M = max m_p, L = sum l_p 2^(m_p - M),
 // out = sum acc_p 2^(m_p - M) / L.  One CTA per (sequence, q-head): the
 // partition maxima and sums are loaded in parallel (one per thread) into
@@ -787,7 +796,12 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     if (n <= 0) return;
     const int n_chunks = (n + kChunk - 1) / kChunk;
     const int c_lo = (p.window > 0 && n > p.window) ? (n - p.window) / kChunk : 0;
-    const int n_parts = min((n_chunks - c_lo + p.part_chunks - 1) / p.part_chunks, p.max_parts);
+    int n_parts = (n_chunks - c_lo + p.part_chunks - 1) / p.part_chunks;
+    if (p.partner != nullptr) {  // shared-prefix decode: pair slots, then own partitions
+        const mma::Pairing pr = mma::pairing_of(p, s, false);
+        n_parts = pr.np_shared + pr.np_priv;
+    }
+    n_parts = min(n_parts, p.max_parts);
     if (n_parts <= 1) return;
     __shared__ float wts[kMergeMaxParts];
     __shared__ float red[kMergeThreads / 32];
@@ -876,12 +890,26 @@ constexpr int kWarps = 4;
 constexpr int kStages = 2;
 constexpr int kWaves = 9;
 
+// The tensor-core partition kernel (decode_mma.cuh) serves bf16 pools with
+// head_dim 128 and pages of >= 16 tokens (a chunk then lies in one page),
+// when the pool's rows fit the int32 row coordinate of its TMA boxes, at
+// G >= 2 query heads per kv-head; MHA (G = 1) and everything else run on
+// the CUDA-core kernel.
+static bool use_mma(const pa_kv_pool* pool, int32_t Hq) {
+    const int G = pool->num_kv_heads > 0 ? Hq / pool->num_kv_heads : 1;
+    return pool->dtype == PA_DTYPE_BF16 && pool->head_dim == mma::kD && pool->block_size >= 16 &&
+           (int64_t)pool->num_blocks * pool->num_kv_heads * pool->block_size <= INT32_MAX &&
+           (G == 2 || G == 4 || G == 8);
+}
+
 // Partition CTAs per SM the plan counts on: 3 (the shared-memory limit of
-// 16-bit and f32 rows), 2 at G = 8, where registers allow only two.  (FP8 rows
-// at G <= 4 run 4 per SM, but measured fastest with the 3-per-SM plan: more
-// partitions cost more in the merge than they gain in balance.)
+// the tensor-core kernel and of 16-bit and f32 rows on the CUDA-core one), 2
+// for the CUDA-core kernel at G = 8, where registers allow only two.  (FP8
+// rows at G <= 4 run 4 per SM, but measured fastest with the 3-per-SM plan:
+// more partitions cost more in the merge than they gain in balance.)
 static int ctas_per_sm(const pa_kv_pool* pool, int32_t Hq) {
     const int G = pool->num_kv_heads > 0 ? Hq / pool->num_kv_heads : 1;
+    if (use_mma(pool, Hq)) return 3;
     return G >= 8 ? 2 : 3;
 }
 
@@ -928,6 +956,20 @@ static pa_status make_plan(const pa_kv_pool* pool, int32_t B, int32_t Hq, int32_
     return PA_OK;
 }
 
+// Plan of the shared-prefix decode: pa_decode's partition size; splitting a
+// context at the shared length adds at most one slot per sequence.
+static pa_status make_shared_plan(const pa_kv_pool* pool, int32_t B, int32_t Hq, int32_t max_ctx,
+                                  int32_t partition_tokens, Plan* plan) {
+    pa_status st = make_plan(pool, B, Hq, max_ctx, partition_tokens, plan, 0);
+    if (st != PA_OK) return st;
+    plan->max_parts += 1;
+    const size_t rows = (size_t)B * Hq * plan->max_parts;
+    plan->off_l = align256(rows * 4);
+    plan->off_acc = plan->off_l + align256(rows * 4);
+    plan->ws_bytes = plan->off_acc + rows * (size_t)pool->head_dim * 4;
+    return PA_OK;
+}
+
 template <typename T, int G, bool kFused>
 static pa_status launch_partial(const DecodeParams& prm, int32_t B, int32_t Hkv, int32_t max_parts,
                                 cudaStream_t stream) {
@@ -956,6 +998,59 @@ static pa_status launch_partial(const DecodeParams& prm, int32_t B, int32_t Hkv,
         return PA_ERR_CUDA;
     }
     return launch_status();
+}
+
+// Tensor maps of the K and V pools viewed as [rows][head_dim] bf16, boxes of
+// 16 rows x 64 dims in the 128-byte swizzle.
+static pa_status pool_maps(const pa_kv_pool* pool, CUtensorMap* mk, CUtensorMap* mv) {
+    const uint64_t rows = (uint64_t)pool->num_blocks * pool->num_kv_heads * pool->block_size;
+    const uint64_t dims[2] = {(uint64_t)mma::kD, rows};
+    const uint64_t strides[1] = {(uint64_t)mma::kD * 2};
+    const uint32_t box[2] = {64, (uint32_t)kChunk};
+    if (!encode_bf16_map_sw128(mk, pool->k_pool, 2, dims, strides, box) ||
+        !encode_bf16_map_sw128(mv, pool->v_pool, 2, dims, strides, box))
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+template <typename K>
+static pa_status launch_mma(K kern, const pa_kv_pool* pool, const DecodeParams& prm, int32_t B,
+                            int32_t max_parts, bool* attr_done, cudaStream_t stream) {
+    CUtensorMap mk, mv;
+    pa_status st = pool_maps(pool, &mk, &mv);
+    if (st != PA_OK) return st;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)mma::kSmem);
+        if (e != cudaSuccess) {
+            record_cuda_error(e);
+            return PA_ERR_CUDA;
+        }
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    cudaError_t e = launch_pdl(kern, dim3((unsigned)B, (unsigned)pool->num_kv_heads, (unsigned)max_parts),
+                               dim3(mma::kW * 32), mma::kSmem, stream, prm, mk, mv);
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PA_ERR_CUDA;
+    }
+    return launch_status();
+}
+
+template <int G>
+static pa_status launch_partial_mma(const pa_kv_pool* pool, const DecodeParams& prm, int32_t B,
+                                    int32_t max_parts, cudaStream_t stream) {
+    static bool attr_done[64] = {false};
+    return launch_mma(mma::decode_mma_kernel<G>, pool, prm, B, max_parts, attr_done, stream);
+}
+
+template <int G>
+static pa_status launch_shared_mma(const pa_kv_pool* pool, const DecodeParams& prm, int32_t B,
+                                   int32_t max_parts, cudaStream_t stream) {
+    static bool attr_done[64] = {false};
+    return launch_mma(mma::decode_shared_kernel<G>, pool, prm, B, max_parts, attr_done, stream);
 }
 
 template <typename T, bool kFused>
@@ -1063,6 +1158,14 @@ static pa_status decode_partial_impl(const pa_kv_pool* pool, const void* q, int3
     prm.k_scale = fp8 ? static_cast<const float*>(pool->k_scale) : nullptr;
     prm.v_scale = fp8 ? static_cast<const float*>(pool->v_scale) : nullptr;
     cudaStream_t cs = (cudaStream_t)stream;
+    if (use_mma(pool, num_q_heads)) {
+        switch (G) {
+            case 2: return launch_partial_mma<2>(pool, prm, num_seqs, plan.max_parts, cs);
+            case 4: return launch_partial_mma<4>(pool, prm, num_seqs, plan.max_parts, cs);
+            case 8: return launch_partial_mma<8>(pool, prm, num_seqs, plan.max_parts, cs);
+            default: return PA_ERR_UNSUPPORTED;
+        }
+    }
     if (fp8)
         return dispatch_group<uint8_t, false>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
     if (pool->dtype == PA_DTYPE_F32)
@@ -1074,14 +1177,16 @@ static pa_status decode_merge_impl(const pa_kv_pool* pool, int32_t num_q_heads,
                                    const int32_t* context_lens, int32_t num_seqs,
                                    int32_t max_context, int32_t window, int32_t partition_tokens,
                                    float* out, void* workspace, size_t workspace_bytes,
-                                   pa_stream_t stream) {
+                                   pa_stream_t stream, const int32_t* partner = nullptr,
+                                   const int32_t* shared_lens = nullptr) {
     pa_status st = check_pool(pool);
     if (st != PA_OK) return st;
     if (num_seqs < 0 || num_q_heads <= 0 || max_context < 0) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
     if (!context_lens || !out) return PA_ERR_INVALID_ARG;
     Plan plan;
-    st = make_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan, window);
+    st = partner ? make_shared_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan)
+                 : make_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan, window);
     if (st != PA_OK) return st;
     if (plan.max_parts <= 1) return PA_OK;
     if (workspace == nullptr || workspace_bytes < plan.ws_bytes || !aligned16(workspace))
@@ -1095,6 +1200,10 @@ static pa_status decode_merge_impl(const pa_kv_pool* pool, int32_t num_q_heads,
     prm.window = window;
     prm.out = out;
     bind_workspace(plan, workspace, &prm);
+    prm.log2_bp = ilog2(pool->block_size);
+    prm.partner = partner;
+    prm.shared_lens = shared_lens;
+    prm.num_seqs = num_seqs;
     const int D = pool->head_dim;
     cudaError_t e = launch_pdl(decode_merge_kernel, dim3((unsigned)((int64_t)num_seqs * num_q_heads)),
                                dim3(kMergeThreads), 0, (cudaStream_t)stream, prm, D);
@@ -1253,4 +1362,88 @@ extern "C" pa_status pa_decode_window(const pa_kv_pool* pool, const void* q, int
     if (st != PA_OK) return st;
     return decode_merge_impl(pool, num_q_heads, context_lens, num_seqs, max_context, window,
                              partition_tokens, out, workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------- shared prefixes
+static bool shared_supported(const pa_kv_pool* pool, int32_t Hq) {
+    const int G = Hq / pool->num_kv_heads;
+    return pool->dtype == PA_DTYPE_BF16 && pool->head_dim == mma::kD && pool->block_size >= 16 &&
+           is_pow2(pool->block_size) &&
+           (int64_t)pool->num_blocks * pool->num_kv_heads * pool->block_size <= INT32_MAX &&
+           (G == 1 || G == 2 || G == 4 || G == 8);
+}
+
+extern "C" pa_status pa_decode_shared_workspace_bytes(const pa_kv_pool* pool, int32_t num_seqs,
+                                                      int32_t num_q_heads, int32_t max_context,
+                                                      int32_t partition_tokens, size_t* bytes) {
+    pa_status st = check_pool(pool);
+    if (st != PA_OK) return st;
+    if (!bytes) return PA_ERR_INVALID_ARG;
+    Plan plan;
+    st = make_shared_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan);
+    if (st != PA_OK) return st;
+    *bytes = plan.ws_bytes;
+    return PA_OK;
+}
+
+extern "C" pa_status pa_decode_shared(const pa_kv_pool* pool, const void* q, int32_t num_q_heads,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t num_seqs,
+                                      int32_t max_context, const int32_t* partner,
+                                      const int32_t* shared_lens, float scale,
+                                      int32_t partition_tokens, float* out, void* workspace,
+                                      size_t workspace_bytes, int32_t* d_err, pa_stream_t stream) {
+    pa_status st = check_pool(pool);
+    if (st != PA_OK) return st;
+    if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq < 0 || max_context < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!q || !block_tables || !context_lens || !out || !partner || !shared_lens)
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % pool->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return PA_ERR_INVALID_ARG;
+    if (!shared_supported(pool, num_q_heads)) return PA_ERR_UNSUPPORTED;
+    if (pool->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(pool->k_pool) || !aligned16(pool->v_pool))
+        return PA_ERR_INVALID_ARG;
+    const int G = num_q_heads / pool->num_kv_heads;
+    Plan plan;
+    st = make_shared_plan(pool, num_seqs, num_q_heads, max_context, partition_tokens, &plan);
+    if (st != PA_OK) return st;
+    if (plan.max_parts > 65535) return PA_ERR_UNSUPPORTED;
+    if (workspace == nullptr || workspace_bytes < plan.ws_bytes || !aligned16(workspace))
+        return PA_ERR_INVALID_ARG;
+    DecodeParams prm = {};
+    prm.k_pool = static_cast<const unsigned char*>(pool->k_pool);
+    prm.v_pool = static_cast<const unsigned char*>(pool->v_pool);
+    prm.num_blocks = pool->num_blocks;
+    prm.log2_bp = ilog2(pool->block_size);
+    prm.num_kv_heads = pool->num_kv_heads;
+    prm.q = q;
+    prm.num_q_heads = num_q_heads;
+    prm.block_tables = block_tables;
+    prm.max_blocks = max_blocks_per_seq;
+    prm.context_lens = context_lens;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.part_chunks = plan.part_chunks;
+    prm.max_parts = plan.max_parts;
+    prm.max_context = max_context;
+    prm.out = out;
+    bind_workspace(plan, workspace, &prm);
+    prm.d_err = d_err;
+    prm.partner = partner;
+    prm.shared_lens = shared_lens;
+    prm.num_seqs = num_seqs;
+    cudaStream_t cs = (cudaStream_t)stream;
+    switch (G) {
+        case 1: st = launch_shared_mma<1>(pool, prm, num_seqs, plan.max_parts, cs); break;
+        case 2: st = launch_shared_mma<2>(pool, prm, num_seqs, plan.max_parts, cs); break;
+        case 4: st = launch_shared_mma<4>(pool, prm, num_seqs, plan.max_parts, cs); break;
+        case 8: st = launch_shared_mma<8>(pool, prm, num_seqs, plan.max_parts, cs); break;
+        default: return PA_ERR_UNSUPPORTED;
+    }
+    if (st != PA_OK) return st;
+    return decode_merge_impl(pool, num_q_heads, context_lens, num_seqs, max_context, 0,
+                             partition_tokens, out, workspace, workspace_bytes, stream, partner,
+                             shared_lens);
 }

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/pagedkv.h"
@@ -48,6 +49,13 @@ inline pa_status launch_status() {
 
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();
+
+// Tiled TMA descriptor of a bf16 tensor of rank 2 or 3 with the 128-byte
+// swizzle (dims innermost first, strides in bytes for dims 1.., box in
+// elements), encoded through the driver's cuTensorMapEncodeTiled.  false if
+// the driver entry point is missing or refuses the description.
+bool encode_bf16_map_sw128(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides, const uint32_t* box);
 
 // Launch with programmatic stream serialization (the kernel must call
 // griddep_wait() before touching memory its predecessor may write).

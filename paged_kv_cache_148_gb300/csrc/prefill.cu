@@ -15,11 +15,12 @@
 // through the block table.
 //
 // Roles (384 threads, one CTA per SM):
-//   warp 0      TMA producer: both Q tiles once; K tiles into a 3-stage ring
+//   warp 0      TMA producer: both Q tiles once; K tiles into a 2-stage ring
 //               (a stage frees when the S MMAs of both q-tiles complete) and
-//               V tiles into a 2-stage ring (freed when both P*V MMAs
+//               V tiles into a 3-stage ring (freed when both P*V MMAs
 //               complete).  Lane k handles page k of a tile.
-//   warp 1      MMA issuer (one thread): S_X = Q_X K_j^T into TMEM, then
+//   warp 1      MMA issuer (the whole warp; elect.sync picks the lane that
+//               issues each MMA): S_X = Q_X K_j^T into TMEM, then
 //               O_X += P_X V_j with P_X read from TMEM, alternating A and B so
 //               one q-tile's softmax overlaps the other's MMAs.
 //   warps 2-3   V converters: each K/V tile's V is turned from bf16 into fp16
@@ -33,9 +34,11 @@
 // Q K^T runs on bf16 operands; P V runs on fp16 operands: P in [0, 2^8]
 // keeps 11 significant bits in fp16 against 8 in bf16, which the stated
 // accuracy needs (bf16 P alone leaves ~1.6e-3 relative L2 error at 2.5K
-// keys).  bf16 -> fp16 is exact for |v| <= 65504 (the fp16 range; larger
-// magnitudes saturate to +-65504) apart from fp16 subnormals below 2^-14,
-// whose absolute error stays under 2^-25.
+// keys).  bf16 -> fp16 is exact for |v| <= 65504 (the fp16 range) apart from
+// fp16 subnormals below 2^-14, whose absolute error stays under 2^-25.  Larger
+// magnitudes saturate to +-65504; the converter warps track the largest |v|
+// they convert and store PA_ERR_UNSUPPORTED in *d_err when one was out of
+// range, so such a result never passes silently.
 // All mbarrier waits are bounded; a wait that runs out sets PA_ERR_TIMEOUT
 // and the CTA winds down.
 #include <cuda.h>
@@ -114,6 +117,14 @@ PA_DEVICE uint4 ld_shared_v4(uint32_t addr) {
 PA_DEVICE uint32_t pack_f16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// running magnitude maximum of bf16 pairs: |result| = max(|a|, |b|) per half
+// (the sign bits are not used)
+PA_DEVICE uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
 
@@ -412,6 +423,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     } else if (warp < 4) {
         // ------------------------------------------------------------ V converters
         const int t = (warp - 2) * 32 + lane;  // rows t and t + 64 of every V tile
+        uint32_t vmax = 0;  // largest |V| converted by this thread, as a bf16 pair
         for (int j = 0; j < n_tiles; ++j) {
             if (!pf_wait_warp(&bars->v_full[j % kVStages], (j / kVStages) & 1, bars, p.d_err)) break;
             const uint32_t vbase = smem_u32(smem + kOffV + (j % kVStages) * kTile);
@@ -431,6 +443,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                             x[c] = ld_shared_v4(vrow + hb * kHalf + ((c + r) & 7) * 16);
 #pragma unroll
                         for (int c = 0; c < 8; ++c)
+                            vmax = bf16x2_absmax(vmax, bf16x2_absmax(bf16x2_absmax(x[c].x, x[c].y),
+                                                                     bf16x2_absmax(x[c].z, x[c].w)));
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
                             st_shared_v4(vrow + hb * kHalf + ((c + r) & 7) * 16,
                                          bf16x2_to_f16x2(x[c].x), bf16x2_to_f16x2(x[c].y),
                                          bf16x2_to_f16x2(x[c].z), bf16x2_to_f16x2(x[c].w));
@@ -444,6 +460,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             fence_proxy_async_smem();
             mbar_arrive(&bars->v_ready[j % kVStages]);
         }
+        // a V element beyond the fp16 range (|v| >= 65536, the first bf16 magnitude
+        // above 65504, or an infinity) was saturated by the conversion: the result
+        // is not the attention over the stored values, so say so
+        if ((vmax & 0x7fffu) >= 0x4780u || ((vmax >> 16) & 0x7fffu) >= 0x4780u)
+            set_error(p.d_err, PA_ERR_UNSUPPORTED);
     } else {
         // ------------------------------------------------------------ softmax
         const int x = warp >= 8 ? 1 : 0;           // q-tile A or B
@@ -570,29 +591,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
 }
 
 // ---------------------------------------------------------------- host side
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
 static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
                      const cuuint64_t* strides, const cuuint32_t* box) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
-                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    uint64_t d[3], st[2];
+    uint32_t bx[3];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        if (i > 0) st[i - 1] = strides[i - 1];
+    }
+    return encode_bf16_map_sw128(m, base, rank, d, st, bx);
 }
 
 template <int G>

@@ -1,20 +1,26 @@
 """pa_decode_noalloc: decode with no caller-provided workspace.
 
-Callers that cannot allocate device memory when they run decode (code being
-captured into a CUDA graph, plugin hosts that hand over raw pointers but no
-allocator, processes whose HBM all belongs to the block pool) use this entry
-point; its split-KV scratch lives in a static device array inside the
-library.  The test calls it through the C ABI twice in a row and checks each
-result against pa_decode with an ordinary workspace, within the same bf16
-tolerance as the other decode tests.  It runs on its own in a fresh process
-as well as after the other tests, and is collected last.
+Some callers cannot allocate device memory when they run decode: plugin or
+custom-op hosts that hand over raw device pointers but no allocator, and
+serving processes that give all spare HBM to the block pool.  They use this
+entry point; its split-KV scratch lives in a static device array inside the
+library.  The tests call it through the C ABI twice in a row.  Both calls
+must equal pa_decode with an ordinary workspace bit for bit, since they run
+the same kernels with the same partition plan.  Both must also match the
+float64 oracle within the bf16 decode tolerance.  One test repeats the check
+in a fresh Python process, so it also covers the first call's set-up.  The
+file is collected last.
 """
 import ctypes
+import os
+import subprocess
+import sys
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_148_gb300 as pkv
 import workloads
 from harness import GpuWorkload
@@ -22,6 +28,7 @@ from harness import GpuWorkload
 pytestmark = pytest.mark.gpu
 
 MAX_ABS, REL_L2 = 2e-3, 1e-3
+_CHILD = "PKV_NOALLOC_FRESH_PROCESS"
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -50,19 +57,39 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls():
     assert pkv.decode_workspace_bytes(g.cache.pool, wl.num_seqs, wl.num_q_heads,
                                       g.max_context, part) > 0
     g.set_partition_tokens(part)
+    g.err.zero_()
     ref = g.attend().clone()
     torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    oc = oracle.OracleCache(wl)
+    exact = oracle.decode(oc.k, oc.v, oracle.to_numpy_bits(g.q_host), oc.tables, wl.total_lens,
+                          wl.scale)
     for call in range(2):
         out = torch.full_like(ref, float("nan"))
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         st = _noalloc(g, out, part, err)
         assert st == pkv.PA_OK, pkv.status_str(st)
         torch.cuda.synchronize()
-        assert int(err.item()) == 0
-        a, b = out.cpu().numpy().astype(np.float64), ref.cpu().numpy().astype(np.float64)
+        assert int(err.item()) == 0, pkv.status_str(int(err.item()))
+        assert torch.equal(out, ref), "call %d differs from pa_decode" % call
+        a = out.cpu().numpy().astype(np.float64)
         assert np.isfinite(a).all()
-        assert np.abs(a - b).max() <= MAX_ABS
-        assert np.linalg.norm(a - b) / np.linalg.norm(b) <= REL_L2
+        assert np.abs(a - exact).max() <= MAX_ABS
+        assert np.linalg.norm(a - exact) / np.linalg.norm(exact) <= REL_L2
+
+
+@pytest.mark.skipif(os.environ.get(_CHILD) == "1", reason="already the fresh process")
+def test_noalloc_in_a_fresh_process():
+    """The two-call check again, as the first use of the library in a new process."""
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, **{_CHILD: "1"})
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.abspath(__file__) +
+                        "::test_noalloc_decode_matches_workspace_decode_on_two_calls"],
+                       cwd=os.path.dirname(here), env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
+    assert "1 passed" in r.stdout
 
 
 def test_noalloc_rejects_shapes_beyond_the_static_scratch():

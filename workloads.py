@@ -195,18 +195,28 @@ def decode_mha(scale: float = 1.0) -> Workload:
                     cached, np.ones(B, np.int64), n_blk, order, seed_values=2003)
 
 
-def decode_long_shared(scale: float = 1.0) -> Workload:
+def decode_long_shared(scale: float = 1.0, pairs: str = "adjacent") -> Workload:
+    """pairs: "adjacent" pairs sequences (0, 1), (2, 3), ...; "far" pairs s
+    with s + B/2, so the members of a pair sit half a batch apart."""
     rng = np.random.default_rng(1004)
     B = 8
     lo, hi = max(64, int(32768 * scale)), max(128, int(131072 * scale))
     cached = rng.integers(lo, hi + 1, size=B).astype(np.int64)
-    pair_of = np.array([s ^ 1 for s in range(B)], dtype=np.int64)
+    if pairs == "adjacent":
+        pair_of = np.array([s ^ 1 for s in range(B)], dtype=np.int64)
+    elif pairs == "far":
+        pair_of = np.array([(s + B // 2) % B for s in range(B)], dtype=np.int64)
+    else:
+        raise ValueError("pairs must be 'adjacent' or 'far'")
     prefix = np.zeros(B, np.int64)
-    for a in range(0, B, 2):
-        p = int(math.floor(0.75 * min(cached[a], cached[a + 1])))
+    for a in range(B):
+        b = int(pair_of[a])
+        if a > b:
+            continue
+        p = int(math.floor(0.75 * min(cached[a], cached[b])))
         if p % 16 == 0:
             p -= 1
-        prefix[a] = prefix[a + 1] = p
+        prefix[a] = prefix[b] = p
     # private blocks per member plus the shared ones plus one copy-on-write block per pair
     need = int(_blocks(cached + 1, 16).sum())
     n_blk, order = _pool_for(rng, need, 1.1, minimum=need + 64)
