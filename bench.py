@@ -1,18 +1,26 @@
 #!/usr/bin/env python
 """Benchmark of the paged KV-cache attention hot path; prints ONE JSON line.
 
-A step is one pass of the decode hot path over one batch: pa_write_kv of the
-batch's new K/V rows through slot_mapping, then pa_decode (split-KV
+A decode step is one pass of the decode hot path over one batch: pa_write_kv
+of the batch's new K/V rows through slot_mapping, then pa_decode (split-KV
 partition kernel + merge kernel) reading every visible token through the
-block tables.  The default workload is the GQA decode batch (64 sequences,
-H_q 32 / H_kv 8, head_dim 128, block size 16, bf16, contexts U[128, 4096]).
-``--workload prefill`` times pa_write_kv + pa_prefill instead.
+block tables.  A prefill step is pa_write_kv + pa_prefill.
+
+Default (``--workload suite``): the line's top level is the headline
+configuration, the MHA decode batch (256 sequences, 32/32 heads, head_dim
+128, block size 16, bf16, contexts lognormal(ln 512, 1) clipped to [16,
+2048]; the largest single-GPU decode batch, 2.86 GB of K/V per step).
+``suite`` holds one record per other configuration (the tiny fp32 decode,
+the GQA decode, the long shared-prefix decode also through
+pa_decode_shared, the chunked prefill) and the pa_write_kv / pa_copy_blocks
+microbenchmarks, each with its own value, kernel times, roofline and clocks.
+``--workload NAME`` times one workload only.
 
 Timing: W untimed warm-up steps; then K steps bracketed by CUDA events on the
-launching stream (the step's K/V is larger than L2; ``--l2 flush`` adds a
-256 MiB write before every step, outside its events); barrier + synchronize
-around the loop; max over ranks.  ``--path fused`` times pa_decode_step (one
-launch) and ``--window W`` pa_decode_window (sliding window) instead.
+launching stream; barrier + synchronize around the loop; max over ranks.
+Steps that move less than twice the 129 MB L2 (and ``--l2 flush``) get a
+256 MiB write before every step, outside its events.  ``--path fused`` times
+pa_decode_step (one launch) and ``--window W`` pa_decode_window instead.
 value = algorithmic bytes of all ranks / max step time (GB/s).  The
 algorithmic bytes of a decode step are the K/V rows of every visible token,
 Q, the fp32 output, the block-table entries and context lengths.
@@ -50,17 +58,22 @@ def parse():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode_gqa", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default="suite", choices=["suite"] + sorted(workloads.WORKLOADS),
+                    help="suite (default): the headline decode_mha line with a record per other "
+                         "configuration and the write / copy microbenchmarks; or one workload")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--l2", choices=["none", "flush"], default="none",
                     help="none: the step's K/V (4x the 129 MB L2) is itself larger than L2; "
                          "flush: write a 256 MiB buffer before every timed step")
-    ap.add_argument("--path", choices=["fused", "split"], default="split",
+    ap.add_argument("--scale", type=float, default=1.0,
+                    help="single-workload runs: the workload's size scale (small profiling cases)")
+    ap.add_argument("--path", choices=["fused", "split", "shared"], default="split",
                     help="decode step: split = pa_write_kv + pa_decode_partial + pa_decode_merge "
                          "(dependent launches; fastest on large batches); fused = pa_decode_step "
-                         "(write + attention + merge in one launch; fastest on small batches)")
+                         "(write + attention + merge in one launch; fastest on small batches); "
+                         "shared = pa_write_kv + pa_decode_shared (declared shared-prefix pairs)")
     ap.add_argument("--window", type=int, default=0,
                     help="decode: sliding window in positions (pa_decode_window); 0 = none")
     ap.add_argument("--partition-tokens", type=int, default=0,
@@ -186,6 +199,8 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "decode_partition_kernel": ("decode.cu", "common.cuh"),
     "decode_step": ("decode.cu", "common.cuh"),
+    "decode_mma_kernel": ("decode.cu", "decode_mma.cuh", "tcgen05.cuh", "common.cuh"),
+    "decode_shared_kernel": ("decode.cu", "decode_mma.cuh", "tcgen05.cuh", "common.cuh"),
     "prefill_kernel": ("prefill.cu", "tcgen05.cuh", "common.cuh"),
 }
 
@@ -321,40 +336,104 @@ def aggregate_value(bytes_per_rank: int, world: int, max_ms: float) -> float:
 
 
 # --------------------------------------------------------------------------- GPU arm
-def run_ours(args, rank, world, local_rank):
+L2_BYTES = 129 * 10**6
+HEADLINE = "decode_mha"
+SUITE = ["decode_tiny", "decode_gqa", "decode_long_shared", "prefill"]
+DECODE_PATH = {"split": "split: pa_write_kv + pa_decode_partial + pa_decode_merge",
+               "fused": "fused: pa_decode_step (new-token write, attention and split-KV merge in "
+                        "one launch)",
+               "window": "pa_write_kv + pa_decode_window (partition + merge)",
+               "shared": "pa_write_kv + pa_decode_shared (shared-prefix pair units + own "
+                         "partitions, then the merge)"}
+
+
+def _events(torch, n, k):
+    return [[torch.cuda.Event(enable_timing=True) for _ in range(k)] for _ in range(n)]
+
+
+def _needs_flush(args, step_bytes: int) -> bool:
+    """Flush L2 between timed steps when asked, or when one step's bytes would
+    not push the previous step's data out of the 129 MB L2 by themselves."""
+    return args.l2 == "flush" or step_bytes < 2 * L2_BYTES
+
+
+def _l2_note(flush: bool, step_bytes: int) -> str:
+    if flush:
+        return "flushed before every timed step by a 256 MiB write outside the step's events"
+    return ("no flush: inputs larger than L2 (one step moves %.0f MB, L2 is 129 MB)"
+            % (step_bytes / 1e6))
+
+
+def _shared_inputs(torch, wl, dev):
+    """partner / shared_lens of the workload's declared pairs (whole shared pages)."""
+    B = wl.num_seqs
+    partner = np.full(B, -1, np.int32)
+    shared = np.zeros(B, np.int32)
+    if wl.pair_of is not None:
+        for s in range(B):
+            q = int(wl.pair_of[s])
+            if q >= 0:
+                partner[s] = q
+                shared[s] = int(wl.prefix_len[s]) // wl.block_size * wl.block_size
+    return (torch.from_numpy(partner).to(dev), torch.from_numpy(shared).to(dev))
+
+
+def bench_attention(args, wl, dev, world, mode="split", e2e=False, g=None):
+    """One configuration: loop A times whole steps (value, ms_per_step, clocks),
+    loop B puts an event between the kernels of each step (kernel_ms, the
+    roofline of the dominant kernel).  Returns the record and the workload."""
     import torch
-    import torch.distributed as dist
     import paged_kv_cache_148_gb300 as pkv
     from harness import GpuWorkload
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    pkv.build()
-    wl = workloads.WORKLOADS[args.workload]()
-    g = GpuWorkload(wl, device=dev)
-    if args.partition_tokens:
-        g.set_partition_tokens(args.partition_tokens)
+    if g is None:
+        g = GpuWorkload(wl, device=dev)
+        if args.partition_tokens:
+            g.set_partition_tokens(args.partition_tokens)
     stream = torch.cuda.current_stream(dev)
     is_decode = wl.kind == "decode"
-    window = args.window if is_decode else 0
+    window = args.window if (is_decode and mode == "window") else 0
     if window > 0:
         g.set_window(window)
-    fused = is_decode and args.path == "fused" and window == 0
+    fused = is_decode and mode == "fused"
+    shared = None
+    if is_decode and mode == "shared":
+        partner, shared_lens = _shared_inputs(torch, wl, dev)
+        ws_bytes = pkv.decode_shared_workspace_bytes(g.cache.pool, wl.num_seqs, wl.num_q_heads,
+                                                     g.max_context, g.partition_tokens)
+        shared = (partner, shared_lens, torch.empty(max(ws_bytes, 16), dtype=torch.uint8,
+                                                    device=dev))
     max_parts = g.max_parts()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ab = algorithmic_bytes(wl, window)
+    step_bytes = ab["decode_total"] + ab["write"] if is_decode else ab["kv"] + ab["q"] + ab["out"]
+    do_flush = _needs_flush(args, step_bytes)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if do_flush else None
 
-    def step():
-        if fused:
-            g.step(stream, fused=True)
-            return
-        g.write_new(stream)
-        if is_decode and window == 0:
-            g.attend(stream, "partial")
-            g.attend(stream, "merge")
+    def attend():
+        if shared is not None:
+            pkv.decode_shared(g.cache.pool, g.q, g.block_tables, g.context_lens, g.max_context,
+                              shared[0], shared[1], wl.scale, out=g.out, workspace=shared[2],
+                              partition_tokens=g.partition_tokens, d_err=g.err, stream=stream)
         else:
             g.attend(stream)
 
-    do_flush = args.l2 == "flush"
+    # kernels of one step, in launch order (events go between them in loop B)
+    if fused:
+        phases = [("decode_step", lambda: g.step(stream, fused=True))]
+    elif is_decode and mode == "split":
+        phases = [("write_kv", lambda: g.write_new(stream)),
+                  ("decode_partition", lambda: g.attend(stream, "partial")),
+                  ("decode_merge", lambda: g.attend(stream, "merge"))]
+    elif is_decode:
+        phases = [("write_kv", lambda: g.write_new(stream)),
+                  ("decode_%s (partition + merge)" % mode, attend)]
+    else:
+        phases = [("write_kv", lambda: g.write_new(stream)), ("prefill", attend)]
+
+    def step():
+        for _, fn in phases:
+            fn()
+
     for i in range(args.warmup):
         if do_flush:
             flush.fill_(i & 255)
@@ -362,14 +441,12 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     g.err.zero_()
     K = args.steps
-    # loop A: events only around whole steps (kernels inside a step run back to
-    # back, so dependent launches can overlap) -> value, ms_per_step
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
+    ev = _events(torch, K, 2)
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(dev.index or 0)
     clocks.start()
     for i in range(K):
         if do_flush:
@@ -382,48 +459,28 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     step_ms = np.array([a.elapsed_time(b) for a, b in ev])
-    # loop B: an event between every kernel -> each kernel's own time (roofline)
     KB = min(K, 500)
-    evk = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KB)]
+    evk = _events(torch, KB, len(phases) + 1)
     torch.cuda.synchronize(dev)
     for i in range(KB):
         if do_flush:
             flush.fill_(i & 255)
         e = evk[i]
         e[0].record(stream)
-        if fused:  # one kernel: write + attention + merge
-            e[1].record(stream)
-            g.step(stream, fused=True)
-            e[2].record(stream)
-            e[3].record(stream)
-            continue
-        g.write_new(stream)
-        e[1].record(stream)
-        if is_decode and window == 0:
-            g.attend(stream, "partial")
-            e[2].record(stream)
-            g.attend(stream, "merge")
-        else:
-            g.attend(stream)
-            e[2].record(stream)
-        e[3].record(stream)
+        for j, (_, fn) in enumerate(phases):
+            fn()
+            e[j + 1].record(stream)
     torch.cuda.synchronize(dev)
     err = int(g.err.item())
     if err:
-        raise RuntimeError("device error during the timed loops: " + pkv.status_str(err))
-    write_ms = np.array([e[0].elapsed_time(e[1]) for e in evk])
-    attn_ms = np.array([e[1].elapsed_time(e[2]) for e in evk])
-    merge_ms = np.array([e[2].elapsed_time(e[3]) for e in evk])
+        raise RuntimeError("%s: device error during the timed loops: %s"
+                           % (wl.name, pkv.status_str(err)))
+    kernel_ms = {name: float(np.mean([e[j].elapsed_time(e[j + 1]) for e in evk]))
+                 for j, (name, _) in enumerate(phases)}
     ms = max_over_ranks(float(step_ms.mean()), world, dev)
-
-    # end-to-end through the public API with host buffers
-    e2e = run_e2e(args, g, stream, dev, is_decode, fused)
-
     hbm_peak, tf_peak, peak_src = measured_peaks()
-    ab = algorithmic_bytes(wl, window)
-    res = {"metric": METRIC, "n_gpus": world, "steps": K, "warmup": args.warmup,
-           "ms_per_step": ms, "scaling": "weak", "vs_baseline": None, "data": "synthetic",
-           "dtype": wl.dtype}
+    rec = {"workload": wl.name, "steps": K, "ms_per_step": ms, "kernel_ms": kernel_ms,
+           "clocks": clk, "l2": _l2_note(do_flush, step_bytes), "dtype": wl.dtype}
     cfg = {"workload": wl.name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
            "block_size": wl.block_size, "num_blocks": wl.num_blocks,
@@ -431,69 +488,199 @@ def run_ours(args, rank, world, local_rank):
                                                       int(wl.total_lens.min()),
                                                       int(wl.total_lens.max())),
            "per_rank": "each rank runs its own copy of the batch (independent replicas)",
-           "l2": ("flushed before every timed step by a 256 MiB write outside the step's events"
-                  if do_flush else
-                  "no flush: inputs larger than L2 (the step reads %.0f MB of K/V, L2 is 129 MB)"
-                  % (ab_kv_mb(wl, window))),
-           "split_kv_partitions_max": max_parts,
-           "window": window or "none",
-           "path": ("fused: pa_decode_step (new-token write, attention and split-KV merge in one "
-                    "launch)" if fused else
-                    "split: pa_write_kv + pa_decode_partial + pa_decode_merge" if is_decode else
-                    "pa_write_kv + pa_prefill"),
-           "partition_tokens": args.partition_tokens or "auto"}
+           "l2": rec["l2"]}
     if is_decode:
-        cfg["kv_bytes"] = {"logical": ab["kv"],
-                           "unique_physical": physical_kv_bytes(wl, g.tables_list(), window),
+        cfg.update({"split_kv_partitions_max": max_parts, "window": window or "none",
+                    "path": DECODE_PATH[mode], "partition_tokens": args.partition_tokens or "auto",
+                    "kernel": kernel_name(wl, mode)})
+        phys = physical_kv_bytes(wl, g.tables_list(), window)
+        cfg["kv_bytes"] = {"logical": ab["kv"], "unique_physical": phys,
                            "counted": "logical (each sequence's pages once per sequence)"}
         per_rank = ab["decode_total"]
-        res.update({"value": aggregate_value(per_rank, world, ms), "unit": "GB/s",
-                    "higher_is_better": True,
+        rec.update({"value": aggregate_value(per_rank, world, ms), "unit": "GB/s",
                     "tokens_per_s": world * wl.num_seqs / (ms * 1e-3),
                     "pct_of_hbm_peak": 100.0 * (per_rank / (ms * 1e-3) / 1e9) / hbm_peak,
                     "pct_of_nominal_8tbs": 100.0 * (per_rank / (ms * 1e-3) / 1e9) / 8000.0})
-        part_ms = float(attn_ms.mean())
-        achieved = per_rank / (part_ms * 1e-3) / 1e9
-        kname = "decode_step" if fused else "decode_partition_kernel"
-        res["roofline"] = {"kernel": ("decode_partition_kernel (fused step)" if fused else kname),
-                           "bound": "hbm",
-                           "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                           "frac": achieved / hbm_peak, "peak_source": peak_src + " hbm_gbs",
-                           "traffic": None if window else recorded_traffic(kname, wl.name),
-                           "algorithmic_bytes": per_rank, "launch_ms": part_ms}
+        if ab["kv"] != phys:
+            rec["value_physical"] = aggregate_value(per_rank - ab["kv"] + phys, world, ms)
+        dom = "decode_step" if fused else ("decode_partition" if mode == "split" else phases[-1][0])
+        launch_ms = kernel_ms[dom]
+        achieved = per_rank / (launch_ms * 1e-3) / 1e9
+        kname = kernel_name(wl, mode)
+        rec["roofline"] = {"kernel": kname, "bound": "hbm", "achieved": achieved,
+                           "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                           "peak_source": peak_src + " hbm_gbs (copy, burst)",
+                           "traffic": recorded_traffic(kname, wl.name + ("" if mode == "split"
+                                                                         else "_" + mode)),
+                           "algorithmic_bytes": per_rank, "launch_ms": launch_ms,
+                           "timed": "%s%s" % (dom, "" if mode == "split" else
+                                              " (all of its kernels)")}
+        # write + partition kernel, + the merge when a context spans partitions
+        # (the shared-prefix plan always has room for one more slot, so it merges)
         if fused:
-            res["kernel_ms"] = {"decode_step": part_ms}
             launches = K
         else:
-            if window:
-                res["kernel_ms"] = {"write_kv": float(write_ms.mean()),
-                                    "decode_window (partition + merge)": part_ms}
-            else:
-                res["kernel_ms"] = {"write_kv": float(write_ms.mean()), "decode_partition": part_ms,
-                                    "decode_merge": float(merge_ms.mean())}
-            launches = K * (2 + (1 if max_parts > 1 else 0))
+            launches = K * (2 + (1 if (max_parts > 1 or mode == "shared") else 0))
     else:
         flops = prefill_flops(wl)
-        res.update({"metric": "paged chunked-prefill TFLOP/s (causal-visible) on 1 GB300",
-                    "value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                    "higher_is_better": True,
+        rec.update({"value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "tokens_per_s": world * int(wl.new_lens.sum()) / (ms * 1e-3)})
-        pf_ms = float(attn_ms.mean())
+        pf_ms = kernel_ms["prefill"]
         achieved = flops / (pf_ms * 1e-3) / 1e12
-        res["roofline"] = {"kernel": "prefill_kernel", "bound": "tensor", "achieved": achieved,
+        rec["roofline"] = {"kernel": "prefill_kernel", "bound": "tensor", "achieved": achieved,
                            "peak": tf_peak, "unit": "TFLOP/s", "frac": achieved / tf_peak,
                            "peak_source": peak_src + " bf16_tflops (burst)",
                            "traffic": recorded_traffic("prefill_kernel", wl.name),
                            "algorithmic_flops": flops, "launch_ms": pf_ms}
-        res["kernel_ms"] = {"write_kv": float(write_ms.mean()), "prefill": pf_ms}
+        cfg["path"] = "pa_write_kv + pa_prefill"
         launches = K * 2
-    res["gpu_launches"] = launches  # in the timed step loop (loop A)
-    res["kernel_timing"] = ("kernel_ms and roofline.launch_ms come from a second loop of %d steps "
-                            "with an event between every kernel" % KB)
-    res["e2e"] = e2e
-    res["clocks"] = clk
-    res["config"] = cfg
-    return res, wl, ab
+    rec["gpu_launches"] = launches
+    rec["config"] = cfg
+    if e2e:
+        rec["e2e"] = run_e2e(args, g, stream, dev, is_decode, fused)
+    return rec, g
+
+
+def kernel_name(wl, mode="split") -> str:
+    """The library kernel that dominates a decode step of this workload."""
+    if wl.kind != "decode":
+        return "prefill_kernel"
+    if mode == "fused":
+        return "decode_step"
+    if mode == "shared":
+        return "decode_shared_kernel"
+    G = wl.num_q_heads // wl.num_kv_heads
+    if (wl.dtype == "bf16" and getattr(wl, "kv_format", "native") == "native"
+            and wl.head_dim == 128 and wl.block_size >= 16 and G in (2, 4, 8)):
+        return "decode_mma_kernel"
+    return "decode_partition_kernel"
+
+
+def bench_write(args, wl, dev, world):
+    """pa_write_kv of one prefill batch's new rows (8192 rows of K and V)."""
+    import torch
+    from harness import GpuWorkload
+    g = GpuWorkload(wl, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ab = algorithmic_bytes(wl)
+    return _micro(args, dev, world, "write_kv_kernel", ab["write"],
+                  lambda: g.write_new(stream), g.err,
+                  {"workload": wl.name + " new rows", "rows": int(wl.new_lens.sum()),
+                   "row_bytes": wl.num_kv_heads * wl.head_dim * wl.elem_bytes,
+                   "bytes": "K and V rows read and written + 8-byte slots"})
+
+
+def bench_copy(args, dev, world):
+    """pa_copy_blocks of 10% of a decode_gqa-shaped pool, random src != dst."""
+    import torch
+    import paged_kv_cache_148_gb300 as pkv
+    wl = workloads.decode_gqa()
+    pool = pkv.KVPool(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim,
+                      wl.torch_dtype, dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3)
+    for t in (pool.k, pool.v):
+        t.view(torch.int16).random_(generator=gen)
+    rng = np.random.default_rng(1102)
+    n = wl.num_blocks // 10
+    ids = rng.permutation(wl.num_blocks)
+    src = torch.from_numpy(ids[:n].astype(np.int32)).to(dev)
+    dst = torch.from_numpy(ids[n:2 * n].astype(np.int32)).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    page = wl.num_kv_heads * wl.block_size * wl.head_dim * wl.elem_bytes
+    nbytes = 2 * n * page * 2 + 2 * n * 4
+    rec = _micro(args, dev, world, "copy_blocks_kernel", nbytes,
+                 lambda: pkv.copy_blocks(pool, src, dst, d_err=err, stream=stream), err,
+                 {"workload": "decode_gqa-shaped pool (%d blocks), %d pairs" % (wl.num_blocks, n),
+                  "page_bytes": page,
+                  "bytes": "K and V pages read and written + 8 bytes of ids per pair"})
+    del pool
+    return rec
+
+
+def _micro(args, dev, world, kname, nbytes, fn, err, cfg):
+    import torch
+    import paged_kv_cache_148_gb300 as pkv
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for i in range(max(args.warmup, 3)):
+        flush.fill_(i & 255)
+        fn()
+    torch.cuda.synchronize(dev)
+    err.zero_()
+    K = args.steps
+    ev = _events(torch, K, 2)
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    for i in range(K):
+        flush.fill_(i & 255)
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    e = int(err.item())
+    if e:
+        raise RuntimeError("%s: device error: %s" % (kname, pkv.status_str(e)))
+    ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev])), world, dev)
+    hbm_peak, _, peak_src = measured_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    cfg["l2"] = _l2_note(True, nbytes)
+    return {"workload": cfg["workload"], "steps": K, "ms_per_step": ms, "value": world * gbs,
+            "unit": "GB/s", "kernel_ms": {kname: ms}, "clocks": clk, "gpu_launches": K,
+            "roofline": {"kernel": kname, "bound": "hbm", "achieved": gbs, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": gbs / hbm_peak,
+                         "peak_source": peak_src + " hbm_gbs (copy, burst)",
+                         "traffic": None, "algorithmic_bytes": nbytes, "launch_ms": ms},
+            "config": cfg}
+
+
+def run_ours(args, rank, world, local_rank):
+    """The headline configuration (its record is the line's top level) and,
+    for the default suite, one record per other configuration plus the
+    shared-prefix decode and the write / copy microbenchmarks."""
+    import torch
+    import paged_kv_cache_148_gb300 as pkv
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pkv.build()
+    name = HEADLINE if args.workload == "suite" else args.workload
+    mode = args.path if args.path != "split" else ("window" if args.window > 0 else "split")
+    wl = (workloads.WORKLOADS[name]() if args.workload == "suite"
+          else workloads.WORKLOADS[name](args.scale))
+    head, g = bench_attention(args, wl, dev, world, mode, e2e=True)
+    del g
+    torch.cuda.empty_cache()
+    res = {"metric": METRIC if wl.kind == "decode" else
+           "paged chunked-prefill TFLOP/s (causal-visible) on 1 GB300",
+           "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "data": "synthetic", "dtype": head["dtype"]}
+    for k in ("tokens_per_s", "pct_of_hbm_peak", "pct_of_nominal_8tbs", "roofline",
+              "kernel_ms", "gpu_launches", "e2e", "clocks", "config"):
+        if k in head:
+            res[k] = head[k]
+    res["kernel_timing"] = ("kernel_ms and roofline.launch_ms come from a second loop of %d "
+                            "steps with an event between every kernel" % min(args.steps, 500))
+    if args.workload == "suite":
+        suite = {}
+        for other in SUITE:
+            owl = workloads.WORKLOADS[other]()
+            rec, g = bench_attention(args, owl, dev, world, "split")
+            suite[other] = rec
+            if other == "decode_long_shared":
+                rec2, _ = bench_attention(args, owl, dev, world, "shared", g=g)
+                suite["decode_long_shared (shared-prefix decode)"] = rec2
+            if other == "prefill":
+                suite["write_kv (prefill rows)"] = bench_write(args, owl, dev, world)
+            del g
+            torch.cuda.empty_cache()
+        suite["copy_blocks (10% of a decode_gqa pool)"] = bench_copy(args, dev, world)
+        torch.cuda.empty_cache()
+        res["suite"] = suite
+    return res, wl
 
 
 def run_e2e(args, g, stream, dev, is_decode, fused=False):
@@ -554,7 +741,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        wl = workloads.WORKLOADS[args.workload]()
+        wl = workloads.WORKLOADS[HEADLINE if args.workload == "suite" else args.workload]()
         cpu = reference_steps(wl, args.warmup, args.steps, budget_s=150.0)
         line = {"impl": "reference", "metric": METRIC if wl.kind == "decode" else
                 "paged chunked-prefill TFLOP/s (causal-visible) on 1 GB300",
@@ -572,7 +759,7 @@ def main():
     import torch.distributed as dist
     if world > 1:
         dist.init_process_group("nccl")
-    res, wl, ab = run_ours(args, rank, world, local_rank)
+    res, wl = run_ours(args, rank, world, local_rank)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_run(wl, args.cpu_seconds)
         res["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
