@@ -14,7 +14,7 @@
 // page half (64 dims) fetched by one tiled TMA load straight from the pool
 // through the block table.
 //
-// Roles (384 threads, one CTA per SM):
+// Roles (320 threads, one CTA per SM):
 //   warp 0      TMA producer: both Q tiles once; K tiles into a 2-stage ring
 //               (a stage frees when the S MMAs of both q-tiles complete) and
 //               V tiles into a 3-stage ring (freed when both P*V MMAs
@@ -23,22 +23,27 @@
 //               issues each MMA): S_X = Q_X K_j^T into TMEM, then
 //               O_X += P_X V_j with P_X read from TMEM, alternating A and B so
 //               one q-tile's softmax overlaps the other's MMAs.
-//   warps 2-3   V converters: each K/V tile's V is turned from bf16 into fp16
-//               in place (rows past the written keys become zeros).
-//   warps 4-7   softmax of q-tile A, warps 8-11 softmax of q-tile B: thread r
+//   warps 2-5   softmax of q-tile A, warps 6-9 softmax of q-tile B: thread r
 //               owns row r (TMEM lane r): two passes over S_j in TMEM (row max,
 //               then exponentials), base-2 online softmax with lazy rescaling
 //               of O (only when the row max grows by more than 2^8), P_j
 //               written as fp16 pairs into TMEM over the S columns already
 //               read, and finally O / l to global memory.
+//               Between tiles the softmax warps of one q-tile also turn the
+//               next V tile from bf16 into fp16 in place (thread r converts
+//               row r; rows past the written keys become zeros): after
+//               publishing P_X(j) they wait ~half a tile for S_X(j+1), and the
+//               conversion fills that wait on all four SM sub-partitions.  V
+//               tiles alternate between the two q-tiles (the one that still
+//               has tiles takes them all).
 // Q K^T runs on bf16 operands; P V runs on fp16 operands: P in [0, 2^8]
 // keeps 11 significant bits in fp16 against 8 in bf16, which the stated
 // accuracy needs (bf16 P alone leaves ~1.6e-3 relative L2 error at 2.5K
 // keys).  bf16 -> fp16 is exact for |v| <= 65504 (the fp16 range) apart from
 // fp16 subnormals below 2^-14, whose absolute error stays under 2^-25.  Larger
-// magnitudes saturate to +-65504; the converter warps track the largest |v|
-// they convert and store PA_ERR_UNSUPPORTED in *d_err when one was out of
-// range, so such a result never passes silently.
+// magnitudes saturate to +-65504; the threads that convert V track the
+// largest |v| they convert and store PA_ERR_UNSUPPORTED in *d_err when one
+// was out of range, so such a result never passes silently.
 // All mbarrier waits are bounded; a wait that runs out sets PA_ERR_TIMEOUT
 // and the CTA winds down.
 #include <cuda.h>
@@ -58,7 +63,7 @@ constexpr int kPfKeys = 128;            // N: keys per KV tile
 constexpr int kPfDim = 128;             // head_dim
 constexpr int kHalf = 128 * 128;        // bytes of one 64-column half of a 128-row 16-bit tile
 constexpr int kTile = 2 * kHalf;        // 32 KiB
-constexpr int kPfThreads = 384;
+constexpr int kPfThreads = 320;
 constexpr uint32_t kTmemCols = 512;     // S_A | S_B | O_A | O_B
 constexpr float kPfRescale = 8.0f;
 
@@ -93,7 +98,7 @@ struct PfBars {
     uint64_t k_empty[kKStages];
     uint64_t v_full[kVStages];
     uint64_t v_empty[kVStages];
-    uint64_t v_ready[kVStages];     // V converted to fp16 (64 converter threads)
+    uint64_t v_ready[kVStages];     // V converted to fp16 (one q-tile's 128 softmax threads)
     uint64_t s_full[2];             // per q-tile: S_j in TMEM
     uint64_t p_full[2][2];          // per q-tile and half of the keys: P_j in TMEM (128 threads)
     uint64_t o_done[2];             // per q-tile: P_j V_j accumulated into O
@@ -128,7 +133,7 @@ PA_DEVICE uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
     return r;
 }
 
-// bf16 pair -> fp16 pair (saturating at the fp16 range)
+// bf16 pair -> fp16 pair (round to nearest even, saturating at the fp16 range)
 PA_DEVICE uint32_t bf16x2_to_f16x2(uint32_t w) {
     uint32_t r;
     asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
@@ -237,7 +242,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         for (int i = 0; i < kVStages; ++i) {
             mbar_init(&bars->v_full[i], 1);
             mbar_init(&bars->v_empty[i], 1);
-            mbar_init(&bars->v_ready[i], 64);
+            mbar_init(&bars->v_ready[i], 128);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
@@ -420,55 +425,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             }
         }
         __syncwarp();
-    } else if (warp < 4) {
-        // ------------------------------------------------------------ V converters
-        const int t = (warp - 2) * 32 + lane;  // rows t and t + 64 of every V tile
-        uint32_t vmax = 0;  // largest |V| converted by this thread, as a bf16 pair
-        for (int j = 0; j < n_tiles; ++j) {
-            if (!pf_wait_warp(&bars->v_full[j % kVStages], (j / kVStages) & 1, bars, p.d_err)) break;
-            const uint32_t vbase = smem_u32(smem + kOffV + (j % kVStages) * kTile);
-#pragma unroll
-            for (int half_row = 0; half_row < 2; ++half_row) {
-                const int r = t + 64 * half_row;
-                const uint32_t vrow = vbase + r * 128;
-                if (j * kPfKeys + r < zlim) {
-                    // chunk order rotated by the row: 8 threads of a 128-bit phase hit
-                    // 8 different bank groups.  Eight loads go out before the first
-                    // store so their latencies overlap.
-#pragma unroll
-                    for (int hb = 0; hb < 2; ++hb) {
-                        uint4 x[8];
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            x[c] = ld_shared_v4(vrow + hb * kHalf + ((c + r) & 7) * 16);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            vmax = bf16x2_absmax(vmax, bf16x2_absmax(bf16x2_absmax(x[c].x, x[c].y),
-                                                                     bf16x2_absmax(x[c].z, x[c].w)));
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            st_shared_v4(vrow + hb * kHalf + ((c + r) & 7) * 16,
-                                         bf16x2_to_f16x2(x[c].x), bf16x2_to_f16x2(x[c].y),
-                                         bf16x2_to_f16x2(x[c].z), bf16x2_to_f16x2(x[c].w));
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        st_shared_v4(vrow + (c >> 3) * kHalf + ((c + r) & 7) * 16, 0, 0, 0, 0);
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&bars->v_ready[j % kVStages]);
-        }
-        // a V element beyond the fp16 range (|v| >= 65536, the first bf16 magnitude
-        // above 65504, or an infinity) was saturated by the conversion: the result
-        // is not the attention over the stored values, so say so
-        if ((vmax & 0x7fffu) >= 0x4780u || ((vmax >> 16) & 0x7fffu) >= 0x4780u)
-            set_error(p.d_err, PA_ERR_UNSUPPORTED);
     } else {
         // ------------------------------------------------------------ softmax
-        const int x = warp >= 8 ? 1 : 0;           // q-tile A or B
+        const int x = warp >= 6 ? 1 : 0;           // q-tile A or B
         const int nt_x = x ? nt_b : nt_a;
+        // V_jv is converted by a q-tile that runs tile jv - 1 (tile 0: by A):
+        // A for even jv, B for odd jv, or whichever of them still has tiles
+        auto v_owner = [&](int jv) -> int {
+            const bool a_has = jv == 0 ? nt_a > 0 : jv - 1 < nt_a;
+            const bool b_has = jv == 0 ? false : jv - 1 < nt_b;
+            return (a_has && ((jv & 1) == 0 || !b_has)) ? 0 : 1;
+        };
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;         // tile row == TMEM lane
         const int i = r / G, g = r - i * G;
@@ -480,8 +447,45 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         const uint32_t sX = tS(x) + lane_addr, oX = tO(x) + lane_addr;
         const float sc = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;  // m_used in scaled base-2 units
+        uint32_t vmax = 0;  // largest |V| this thread converted, as a bf16 pair
+        // row r of V tile jv from bf16 to fp16 in place (zeros past the
+        // written keys), then this thread's arrival on v_ready
+        auto convert_v = [&](int jv) -> bool {
+            if (!pf_wait_warp(&bars->v_full[jv % kVStages], (jv / kVStages) & 1, bars, p.d_err))
+                return false;
+            const uint32_t vrow = smem_u32(smem + kOffV + (jv % kVStages) * kTile) + r * 128;
+            if (jv * kPfKeys + r < zlim) {
+                // chunk order rotated by the row: the 8 threads of a 128-bit phase
+                // hit 8 different bank groups; eight loads go out before the
+                // first store so their latencies overlap
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    uint4 xv[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        xv[c] = ld_shared_v4(vrow + hb * kHalf + ((c + r) & 7) * 16);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        vmax = bf16x2_absmax(vmax, bf16x2_absmax(bf16x2_absmax(xv[c].x, xv[c].y),
+                                                                 bf16x2_absmax(xv[c].z, xv[c].w)));
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        st_shared_v4(vrow + hb * kHalf + ((c + r) & 7) * 16,
+                                     bf16x2_to_f16x2(xv[c].x), bf16x2_to_f16x2(xv[c].y),
+                                     bf16x2_to_f16x2(xv[c].z), bf16x2_to_f16x2(xv[c].w));
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    st_shared_v4(vrow + (c >> 3) * kHalf + ((c + r) & 7) * 16, 0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->v_ready[jv % kVStages]);
+            return true;
+        };
         bool ok = true;
-        for (int j = 0; j < nt_x; ++j) {
+        if (n_tiles > 0 && v_owner(0) == x) ok = convert_v(0);
+        for (int j = 0; ok && j < nt_x; ++j) {
             if (!pf_wait_warp(&bars->s_full[x], j & 1, bars, p.d_err)) { ok = false; break; }
             tc::fence_after_sync();
             const int key0 = j * kPfKeys;
@@ -559,7 +563,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 }
             }
             l += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
+            // the wait for S_X(j+1) is this q-tile's share of the V conversion
+            if (j + 1 < n_tiles && v_owner(j + 1) == x && !convert_v(j + 1)) { ok = false; break; }
         }
+        // a V element beyond the fp16 range (|v| >= 65536, the first bf16 magnitude
+        // above 65504, or an infinity) was saturated by the conversion: the result
+        // is not the attention over the stored values, so say so
+        if ((vmax & 0x7fffu) >= 0x4780u || ((vmax >> 16) & 0x7fffu) >= 0x4780u)
+            set_error(p.d_err, PA_ERR_UNSUPPORTED);
         // epilogue: O / l -> out
         if (ok && nt_x > 0) ok = pf_wait_warp(&bars->o_done[x], (nt_x - 1) & 1, bars, p.d_err);
         if (ok && nt_x > 0) {
