@@ -783,11 +783,14 @@ namespace pa {
 // Merge of split-KV partials (P1 §4): M = max m_p, L = sum l_p 2^(m_p - M),
 // out = sum acc_p 2^(m_p - M) / L.  One CTA per (sequence, q-head): the
 // partition maxima and sums are loaded in parallel (one per thread) into
-// shared memory, then every thread sums its output element over the
-// partitions with independent loads.
+// shared memory; for head_dim 64 or 128 and up to 128 partitions each thread
+// sums one float4 column over a quarter (an eighth) of the partitions with
+// all of its loads issued up front, otherwise every thread sums its output
+// element over all partitions.
 constexpr int kMergeThreads = 128;
 constexpr int kMergeMaxParts = 1024;  // partitions handled per pass through shared memory
 
+template <int kPre>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p, int D) {
     const int s = blockIdx.x / p.num_q_heads;
     const int g = blockIdx.x - s * p.num_q_heads;
@@ -807,16 +810,22 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     __shared__ float red[kMergeThreads / 32];
     const int64_t base = ((int64_t)s * p.num_q_heads + g) * p.max_parts;
     const int tid = threadIdx.x;
-    if (n_parts <= kMergeThreads && D <= kMergeThreads) {
-        // one round of loads: thread i holds partition i's max and sum, and every
-        // thread its output element of the first kPre partitions
-        constexpr int kPre = 8;
-        float pre[kPre];
+    if (n_parts <= kMergeThreads && (D == 64 || D == 128)) {
+        // thread t owns float4 column t % (D/4) of the output and the partitions
+        // grp, grp + ngrp, ... (grp = t / (D/4)); the first kPre of them are
+        // loaded up front together with the maxima and sums, so the CTA spends
+        // about one round of load latency; the groups are added at the end
+        const int nvec = D >> 2, ngrp = kMergeThreads / nvec;
+        const int col = tid % nvec, grp = tid / nvec;
+        const float4* a4 = reinterpret_cast<const float4*>(p.ws_acc + base * D) + col;
+        float4 pre[kPre];
 #pragma unroll
-        for (int u = 0; u < kPre; ++u)
-            pre[u] = (u < n_parts && tid < D) ? p.ws_acc[(base + u) * D + tid] : 0.f;
-        const float mi = tid < n_parts ? p.ws_m[base + tid] : -INFINITY;
-        const float li = tid < n_parts ? p.ws_l[base + tid] : 0.f;
+        for (int u = 0; u < kPre; ++u) {
+            const int i = grp + u * ngrp;
+            pre[u] = i < n_parts ? __ldcg(a4 + (int64_t)i * nvec) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const float mi = tid < n_parts ? __ldcg(p.ws_m + base + tid) : -INFINITY;
+        const float li = tid < n_parts ? __ldcg(p.ws_l + base + tid) : 0.f;
         float M = mi;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
@@ -836,14 +845,39 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
         L = 0.f;
 #pragma unroll
         for (int w = 0; w < kMergeThreads / 32; ++w) L += red[w];
-        if (tid < D) {
-            float acc = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int u = 0; u < kPre; ++u) acc = fmaf(pre[u], wts[u], acc);
-            const float* a = p.ws_acc + base * D + tid;
-#pragma unroll 4
-            for (int i = kPre; i < n_parts; ++i) acc = fmaf(a[(int64_t)i * D], wts[i], acc);
-            p.out[((int64_t)s * p.num_q_heads + g) * D + tid] = acc / L;
+        for (int u = 0; u < kPre; ++u) {
+            const int i = grp + u * ngrp;
+            const float w = i < n_parts ? wts[i] : 0.f;
+            acc.x = fmaf(pre[u].x, w, acc.x);
+            acc.y = fmaf(pre[u].y, w, acc.y);
+            acc.z = fmaf(pre[u].z, w, acc.z);
+            acc.w = fmaf(pre[u].w, w, acc.w);
+        }
+        for (int i = grp + kPre * ngrp; i < n_parts; i += ngrp) {
+            const float4 v = __ldcg(a4 + (int64_t)i * nvec);
+            const float w = wts[i];
+            acc.x = fmaf(v.x, w, acc.x);
+            acc.y = fmaf(v.y, w, acc.y);
+            acc.z = fmaf(v.z, w, acc.z);
+            acc.w = fmaf(v.w, w, acc.w);
+        }
+        __shared__ float4 grp_acc[kMergeThreads];
+        grp_acc[tid] = acc;
+        __syncthreads();
+        if (tid < nvec) {
+            float4 t = grp_acc[tid];
+            for (int g2 = 1; g2 < ngrp; ++g2) {
+                const float4 o = grp_acc[g2 * nvec + tid];
+                t.x += o.x;
+                t.y += o.y;
+                t.z += o.z;
+                t.w += o.w;
+            }
+            const float inv = 1.f / L;
+            reinterpret_cast<float4*>(p.out + ((int64_t)s * p.num_q_heads + g) * D)[tid] =
+                make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
         }
         return;
     }
@@ -1205,7 +1239,11 @@ static pa_status decode_merge_impl(const pa_kv_pool* pool, int32_t num_q_heads,
     prm.shared_lens = shared_lens;
     prm.num_seqs = num_seqs;
     const int D = pool->head_dim;
-    cudaError_t e = launch_pdl(decode_merge_kernel, dim3((unsigned)((int64_t)num_seqs * num_q_heads)),
+    // partials prefetched per thread: enough for every partition of the plan
+    // with D/4 threads per partition group; few registers keep more CTAs resident
+    const int groups = kMergeThreads / std::max(1, D / 4);
+    auto kern = plan.max_parts <= 4 * groups ? decode_merge_kernel<4> : decode_merge_kernel<16>;
+    cudaError_t e = launch_pdl(kern, dim3((unsigned)((int64_t)num_seqs * num_q_heads)),
                                dim3(kMergeThreads), 0, (cudaStream_t)stream, prm, D);
     if (e != cudaSuccess) {
         record_cuda_error(e);
