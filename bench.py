@@ -12,14 +12,16 @@ configuration, the MHA decode batch (256 sequences, 32/32 heads, head_dim
 2048]; the largest single-GPU decode batch, 2.86 GB of K/V per step).
 ``suite`` holds one record per other configuration (the tiny fp32 decode,
 the GQA decode, the long shared-prefix decode also through
-pa_decode_shared, the chunked prefill) and the pa_write_kv / pa_copy_blocks
+pa_decode_shared and with FP8 pages, the chunked prefill) and the pa_write_kv / pa_copy_blocks
 microbenchmarks, each with its own value, kernel times, roofline and clocks.
 ``--workload NAME`` times one workload only.
 
 Timing: W untimed warm-up steps; then K steps bracketed by CUDA events on the
 launching stream; barrier + synchronize around the loop; max over ranks.
 Steps that move less than twice the 129 MB L2 (and ``--l2 flush``) get a
-256 MiB write before every step, outside its events.  ``--path fused`` times
+256 MiB write before every step, then a read of the same buffer (so the
+write's dirty lines are written back before the step), both outside its
+events.  ``--path fused`` times
 pa_decode_step (one launch) and ``--window W`` pa_decode_window instead.
 value = algorithmic bytes of all ranks / max step time (GB/s).  The
 algorithmic bytes of a decode step are the K/V rows of every visible token,
@@ -50,6 +52,15 @@ import workloads  # noqa: E402
 
 METRIC = "paged decode KV-read GB/s (% of HBM peak) and decode tokens/s on 1 GB300"
 L2_FLUSH_BYTES = 256 << 20
+
+
+def flush_l2(buf, i: int):
+    """Write a buffer twice the size of L2 (so L2 holds none of the step's
+    data), then read it back so the lines the write left dirty are written
+    back now rather than inside the next timed kernel."""
+    import torch
+    buf.fill_(i & 255)
+    buf.view(torch.int32).sum()
 
 
 def parse():
@@ -196,22 +207,35 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- traffic record
+# The source text each kernel's device code comes from.  decode.cu is taken
+# only up to the include of the tensor-core headers: everything after it is
+# the merge kernel and host code (plans, dispatch), which do not change what a
+# partition kernel reads or writes.
+_DECODE_DEVICE = ("decode.cu", '#include "decode_mma.cuh"')
 KERNEL_SOURCES = {
-    "decode_partition_kernel": ("decode.cu", "common.cuh"),
-    "decode_step": ("decode.cu", "common.cuh"),
-    "decode_mma_kernel": ("decode.cu", "decode_mma.cuh", "tcgen05.cuh", "common.cuh"),
-    "decode_shared_kernel": ("decode.cu", "decode_mma.cuh", "tcgen05.cuh", "common.cuh"),
+    "decode_partition_kernel": (_DECODE_DEVICE, "common.cuh"),
+    "decode_step": (_DECODE_DEVICE, "decode_mma.cuh", "tcgen05.cuh", "common.cuh"),
+    "decode_mma_kernel": (_DECODE_DEVICE, "decode_mma.cuh", "tcgen05.cuh", "common.cuh"),
+    "decode_shared_kernel": (_DECODE_DEVICE, "decode_mma.cuh", "tcgen05.cuh", "common.cuh"),
+    "decode_fp8_mma_kernel": (_DECODE_DEVICE, "decode_mma_fp8.cuh", "common.cuh"),
     "prefill_kernel": ("prefill.cu", "tcgen05.cuh", "common.cuh"),
 }
 
 
 def kernel_source_hash(kernel: str) -> str:
-    """Hash of the sources a kernel is built from (to tell whether a recorded
-    ncu traffic figure still describes the kernel as it is)."""
+    """Hash of the source text a kernel's device code comes from (to tell
+    whether a recorded ncu traffic figure still describes the kernel)."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "paged_kv_cache_148_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    for src in KERNEL_SOURCES[kernel]:
+        name, stop = (src, None) if isinstance(src, str) else src
+        with open(os.path.join(ROOT, "paged_kv_cache_148_gb300", "csrc", name), "rb") as fh:
+            text = fh.read()
+        if stop is not None:
+            cut = text.find(stop.encode())
+            if cut < 0:
+                raise ValueError("%s: marker %r not found" % (name, stop))
+            text = text[:cut]
+        h.update(text)
     return h.hexdigest()[:16]
 
 
@@ -338,7 +362,7 @@ def aggregate_value(bytes_per_rank: int, world: int, max_ms: float) -> float:
 # --------------------------------------------------------------------------- GPU arm
 L2_BYTES = 129 * 10**6
 HEADLINE = "decode_mha"
-SUITE = ["decode_tiny", "decode_gqa", "decode_long_shared", "prefill"]
+SUITE = ["decode_tiny", "decode_gqa", "decode_long_shared", "decode_long_shared_fp8", "prefill"]
 DECODE_PATH = {"split": "split: pa_write_kv + pa_decode_partial + pa_decode_merge",
                "fused": "fused: pa_decode_step (new-token write, attention and split-KV merge in "
                         "one launch)",
@@ -359,7 +383,8 @@ def _needs_flush(args, step_bytes: int) -> bool:
 
 def _l2_note(flush: bool, step_bytes: int) -> str:
     if flush:
-        return "flushed before every timed step by a 256 MiB write outside the step's events"
+        return ("flushed before every timed step by a 256 MiB write and a read of the same "
+                "buffer, outside the step's events")
     return ("no flush: inputs larger than L2 (one step moves %.0f MB, L2 is 129 MB)"
             % (step_bytes / 1e6))
 
@@ -436,7 +461,7 @@ def bench_attention(args, wl, dev, world, mode="split", e2e=False, g=None):
 
     for i in range(args.warmup):
         if do_flush:
-            flush.fill_(i & 255)
+            flush_l2(flush, i)
         step()
     torch.cuda.synchronize(dev)
     g.err.zero_()
@@ -450,7 +475,7 @@ def bench_attention(args, wl, dev, world, mode="split", e2e=False, g=None):
     clocks.start()
     for i in range(K):
         if do_flush:
-            flush.fill_(i & 255)
+            flush_l2(flush, i)
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -464,7 +489,7 @@ def bench_attention(args, wl, dev, world, mode="split", e2e=False, g=None):
     torch.cuda.synchronize(dev)
     for i in range(KB):
         if do_flush:
-            flush.fill_(i & 255)
+            flush_l2(flush, i)
         e = evk[i]
         e[0].record(stream)
         for j, (_, fn) in enumerate(phases):
@@ -480,7 +505,9 @@ def bench_attention(args, wl, dev, world, mode="split", e2e=False, g=None):
     ms = max_over_ranks(float(step_ms.mean()), world, dev)
     hbm_peak, tf_peak, peak_src = measured_peaks()
     rec = {"workload": wl.name, "steps": K, "ms_per_step": ms, "kernel_ms": kernel_ms,
-           "clocks": clk, "l2": _l2_note(do_flush, step_bytes), "dtype": wl.dtype}
+           "clocks": clk, "l2": _l2_note(do_flush, step_bytes),
+           "dtype": ("e4m3 pages (float32 row scales), bf16 queries, f32 arithmetic"
+                     if getattr(wl, "kv_format", "native") == "fp8" else wl.dtype)}
     cfg = {"workload": wl.name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
            "block_size": wl.block_size, "num_blocks": wl.num_blocks,
@@ -550,9 +577,12 @@ def kernel_name(wl, mode="split") -> str:
     if mode == "shared":
         return "decode_shared_kernel"
     G = wl.num_q_heads // wl.num_kv_heads
-    if (wl.dtype == "bf16" and getattr(wl, "kv_format", "native") == "native"
-            and wl.head_dim == 128 and wl.block_size >= 16 and G in (2, 4, 8)):
+    fmt = getattr(wl, "kv_format", "native")
+    if (wl.dtype == "bf16" and fmt == "native" and wl.head_dim == 128 and wl.block_size >= 16
+            and G in (2, 4, 8)):
         return "decode_mma_kernel"
+    if fmt == "fp8" and wl.head_dim == 128 and wl.block_size >= 16 and G == 8:
+        return "decode_fp8_mma_kernel"
     return "decode_partition_kernel"
 
 
@@ -605,7 +635,7 @@ def _micro(args, dev, world, kname, nbytes, fn, err, cfg):
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for i in range(max(args.warmup, 3)):
-        flush.fill_(i & 255)
+        flush_l2(flush, i)
         fn()
     torch.cuda.synchronize(dev)
     err.zero_()
@@ -614,7 +644,7 @@ def _micro(args, dev, world, kname, nbytes, fn, err, cfg):
     clocks = ClockSampler(dev.index or 0)
     clocks.start()
     for i in range(K):
-        flush.fill_(i & 255)
+        flush_l2(flush, i)
         ev[i][0].record(stream)
         fn()
         ev[i][1].record(stream)
@@ -715,7 +745,7 @@ def run_e2e(args, g, stream, dev, is_decode, fused=False):
     ms = []
     for i in range(n):
         if args.l2 == "flush":
-            flush.fill_(i & 255)
+            flush_l2(flush, i)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)

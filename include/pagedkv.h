@@ -349,8 +349,9 @@ pa_status pa_decode_shared(const pa_kv_pool* pool, const void* q, int32_t num_q_
  *                  calls of the same shape, including replays of a captured
  *                  CUDA graph.  Calls that share a workspace must be ordered
  *                  on one stream.
- * Other arguments, limits and errors as pa_decode.  Allocates nothing and
- * enqueues one kernel.
+ * Other arguments, limits, arithmetic and errors as pa_decode (bf16 pools
+ * with D = 128, pages of >= 16 tokens and 2, 4 or 8 q-heads per kv-head run
+ * on tensor cores).  Allocates nothing and enqueues one kernel.
  */
 pa_status pa_decode_step_workspace_bytes(const pa_kv_pool* pool, int32_t num_seqs,
                                          int32_t num_q_heads, int32_t max_context,

@@ -778,6 +778,7 @@ __global__ void __launch_bounds__(W * 32, 4) decode_partition_kernel_4ctas(const
 
 }  // namespace pa
 #include "decode_mma.cuh"
+#include "decode_mma_fp8.cuh"
 namespace pa {
 
 // Merge of split-KV partials (P1 §4): M = max m_p, L = sum l_p 2^(m_p - M),
@@ -1073,11 +1074,43 @@ static pa_status launch_mma(K kern, const pa_kv_pool* pool, const DecodeParams& 
     return launch_status();
 }
 
-template <int G>
+template <int G, bool kFused = false>
 static pa_status launch_partial_mma(const pa_kv_pool* pool, const DecodeParams& prm, int32_t B,
                                     int32_t max_parts, cudaStream_t stream) {
     static bool attr_done[64] = {false};
-    return launch_mma(mma::decode_mma_kernel<G>, pool, prm, B, max_parts, attr_done, stream);
+    return launch_mma(mma::decode_mma_kernel<G, kFused>, pool, prm, B, max_parts, attr_done, stream);
+}
+
+// FP8 pages at G = 8 run on the tensor-core FP8 kernel (decode_mma_fp8.cuh):
+// pages of >= 16 tokens, head_dim 128.
+static bool use_mma_fp8(const pa_kv_pool* pool, int32_t Hq) {
+    const int G = pool->num_kv_heads > 0 ? Hq / pool->num_kv_heads : 1;
+    return pool->dtype == PA_DTYPE_FP8_E4M3 && pool->head_dim == mma8::kD &&
+           pool->block_size >= 16 && G == 8;
+}
+
+static pa_status launch_partial_mma_fp8(const DecodeParams& prm, int32_t B, int32_t Hkv,
+                                        int32_t max_parts, cudaStream_t stream) {
+    auto kern = mma8::decode_fp8_mma_kernel<8>;
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)mma8::kSmem);
+        if (e != cudaSuccess) {
+            record_cuda_error(e);
+            return PA_ERR_CUDA;
+        }
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    cudaError_t e = launch_pdl(kern, dim3((unsigned)B, (unsigned)Hkv, (unsigned)max_parts),
+                               dim3(mma8::kW * 32), mma8::kSmem, stream, prm);
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PA_ERR_CUDA;
+    }
+    return launch_status();
 }
 
 template <int G>
@@ -1200,6 +1233,8 @@ static pa_status decode_partial_impl(const pa_kv_pool* pool, const void* q, int3
             default: return PA_ERR_UNSUPPORTED;
         }
     }
+    if (use_mma_fp8(pool, num_q_heads))
+        return launch_partial_mma_fp8(prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
     if (fp8)
         return dispatch_group<uint8_t, false>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
     if (pool->dtype == PA_DTYPE_F32)
@@ -1366,6 +1401,14 @@ extern "C" pa_status pa_decode_step(const pa_kv_pool* pool, const void* k_new, c
                                                     step_sem_offset(plan))
                        : nullptr;
     cudaStream_t cs = (cudaStream_t)stream;
+    if (use_mma(pool, num_q_heads)) {
+        switch (G) {
+            case 2: return launch_partial_mma<2, true>(pool, prm, num_seqs, plan.max_parts, cs);
+            case 4: return launch_partial_mma<4, true>(pool, prm, num_seqs, plan.max_parts, cs);
+            case 8: return launch_partial_mma<8, true>(pool, prm, num_seqs, plan.max_parts, cs);
+            default: return PA_ERR_UNSUPPORTED;
+        }
+    }
     if (pool->dtype == PA_DTYPE_F32)
         return dispatch_group<float, true>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
     return dispatch_group<uint16_t, true>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);

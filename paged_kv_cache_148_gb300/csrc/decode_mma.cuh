@@ -98,11 +98,26 @@ struct Unit {
     int np_a, np_b;    // slots (partitions) of each sequence; 1: write the output directly
 };
 
+// One-launch step (pa_decode_step): the new token's K and V rows of (s, h),
+// kept in shared memory from the kernel's start until the chunk that holds
+// position n - 1 has landed.
+struct StepRow {
+    uint4 row[32];   // lanes 0-15: K row, 16-31: V row (16 bytes each)
+    int64_t slot;    // slot_mapping[s]
+    int32_t pid;     // table entry of the page holding position n - 1
+};
+
 // Unit body for NH head columns (NH = G: one sequence; NH = 2G: a pair).  The
-// caller has set *aborted = 0 and every thread of the CTA enters.
-template <int G, int NH>
+// caller has set *aborted = 0 and every thread of the CTA enters.  With
+// kFused (pa_decode_step, NH = G) the warp that streams the chunk holding
+// position n - 1 also writes the new token's row into the pool and into that
+// chunk's staged copy, and the last partition of (s, h) to finish merges the
+// partials (n_parts > 1).
+template <int G, int NH, bool kFused = false>
 PA_DEVICE void unit_body(const DecodeParams& p, const CUtensorMap* mk, const CUtensorMap* mv,
-                         unsigned char* smem, int* aborted, const Unit& u) {
+                         unsigned char* smem, int* aborted, const Unit& u,
+                         StepRow* step = nullptr) {
+    static_assert(!kFused || NH == G, "the one-launch step decodes single sequences");
     constexpr int NT = (NH + 7) / 8;  // n-tiles of 8 head columns
     static_assert(NH == G || NH == 2 * G, "one sequence or a pair");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -159,6 +174,23 @@ PA_DEVICE void unit_body(const DecodeParams& p, const CUtensorMap* mk, const CUt
         tc::tma_load_2d(dst + 3 * kBox, mv, 64, y, bar);
     };
 
+    // one-launch step: the owner warp streams the chunk of position n - 1 and
+    // loads the new row now (the loads complete behind the prologue's copies)
+    const int n_chunks = (u.n + kChunk - 1) / kChunk;
+    const int last_chunk = n_chunks - 1;
+    const bool owner = kFused && u.ce == n_chunks && last_chunk >= first &&
+                       (last_chunk - first) % kW == 0;
+    uint4 row_reg = make_uint4(0, 0, 0, 0);
+    if (owner) {
+        const int64_t src = ((int64_t)u.seq_a * p.num_kv_heads + u.h) * kRowBytes + (lane & 15) * 16;
+        row_reg = __ldg(reinterpret_cast<const uint4*>((lane < 16 ? p.k_new : p.v_new) + src));
+        if (lane == 0) {
+            step->slot = __ldg(p.slot_mapping + u.seq_a);
+            const int e = (u.n - 1) >> p.log2_bp;
+            step->pid = e < p.max_blocks ? __ldg(table + e) : -1;
+        }
+    }
+
     // Q^T columns: n-tile t, column 8t + gid; lane (gid, tig) holds dims
     // 32q + 8tig .. +7 of that head for q = 0..3 (zeros for padding columns)
     uint4 qa[NT][4];
@@ -178,6 +210,10 @@ PA_DEVICE void unit_body(const DecodeParams& p, const CUtensorMap* mk, const CUt
     for (int i = 0; i < kS; ++i) {
         const int32_t id = __shfl_sync(kFull, id_reg, i & 31);
         if (lane == 0 && i < my_n) issue(i, id);
+    }
+    if (owner) {
+        step->row[lane] = row_reg;  // kept in shared memory through the loop
+        __syncwarp();               // lane 0's slot and page id are visible to the warp
     }
 
     // O^T accumulators: o[mt][t] = dims 16 mt + gid (0, 1) and + 8 (2, 3) of
@@ -229,6 +265,35 @@ PA_DEVICE void unit_body(const DecodeParams& p, const CUtensorMap* mk, const CUt
                         make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();  // before a later copy refills this stage
+            __syncwarp();
+        }
+        if (owner && first + i * kW == last_chunk) {
+            // the new token: check that its slot is that of position n - 1 under
+            // the table, then store its row to the pool and over the staged
+            // chunk's row (the copy may have read the slot before or after the
+            // store; the attention uses the new row either way)
+            const int pos = u.n - 1;
+            const int64_t bpm = (1 << p.log2_bp) - 1;
+            const int64_t slot = step->slot;
+            const int32_t pid = step->pid;
+            int err = 0;
+            if (slot < 0 || slot >= ((int64_t)p.num_blocks << p.log2_bp))
+                err = PA_ERR_OUT_OF_RANGE;
+            else if (pid < 0 || (slot >> p.log2_bp) != pid || (slot & bpm) != (pos & bpm))
+                err = PA_ERR_INVALID_ARG;  // not the slot of the last position
+            if (err != 0) {
+                if (lane == 0) set_error(p.d_err, err);
+            } else {
+                const uint4 v = step->row[lane];
+                const int64_t prow = ((int64_t)pid * p.num_kv_heads + u.h) * (bpm + 1) + (pos & bpm);
+                unsigned char* pool = const_cast<unsigned char*>(lane < 16 ? p.k_pool : p.v_pool);
+                *reinterpret_cast<uint4*>(pool + prow * kRowBytes + (lane & 15) * 16) = v;
+                // 16-byte unit w of row r of a box sits at w ^ (r & 7) (128-byte swizzle)
+                const int r = pos & (kChunk - 1), unit = lane & 15;
+                unsigned char* box = kst + (lane < 16 ? 0 : 2 * kBox) + (unit >> 3) * kBox;
+                *reinterpret_cast<uint4*>(box + r * 128 + (((unit & 7) ^ (r & 7)) << 4)) = v;
+                fence_proxy_async_smem();  // before a later copy refills this stage
+            }
             __syncwarp();
         }
 
@@ -336,7 +401,17 @@ PA_DEVICE void unit_body(const DecodeParams& p, const CUtensorMap* mk, const CUt
 
     // ---- combine the CTA's warps (reusing the ring) and write
     __syncthreads();
-    if (*aborted) return;
+    if (*aborted) {
+        if constexpr (kFused) {
+            // the step still counts this partition so the group's semaphore
+            // returns to zero (the result is flagged invalid by *d_err)
+            if (u.np_a > 1 && threadIdx.x == 0) {
+                int32_t* sem = p.sem + (int64_t)u.seq_a * p.num_kv_heads + u.h;
+                if (atom_add_acq_rel_gpu(sem, 1) == u.np_a - 1) atomicExch(sem, 0);
+            }
+        }
+        return;
+    }
     constexpr int MOFF = NH * kD, LOFF = NH * kD + NH;
     constexpr int WSTRIDE = NH * kD + ((2 * NH + 3) / 4) * 4;
     static_assert((size_t)kW * WSTRIDE * 4 <= kRing, "the warps' combine fits in the ring");
@@ -386,6 +461,23 @@ PA_DEVICE void unit_body(const DecodeParams& p, const CUtensorMap* mk, const CUt
             }
         }
     }
+    if constexpr (kFused) {
+        if (u.np_a > 1) {
+            // publish this partition's partials and count it: the barrier orders
+            // the CTA's stores before thread 0's release-acquire add; the CTA
+            // that counts last merges (its acquire orders the reads of the
+            // others' partials) and returns the semaphore to zero
+            __shared__ int is_last;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                int32_t* sem = p.sem + (int64_t)u.seq_a * p.num_kv_heads + u.h;
+                is_last = atom_add_acq_rel_gpu(sem, 1) == u.np_a - 1;
+                if (is_last) atomicExch(sem, 0);
+            }
+            __syncthreads();
+            if (is_last) merge_group<G, kD, kW>(p, u.seq_a, u.h, u.np_a, cw);
+        }
+    }
 }
 
 // 1024-aligned dynamic shared memory of a CTA (the 128-byte swizzle wants its
@@ -396,8 +488,8 @@ PA_DEVICE unsigned char* aligned_smem(unsigned char* raw) {
 }
 
 // The partition kernel: CTA = (sequence, kv-head, partition), as the
-// CUDA-core form, same plan and partials.
-template <int G>
+// CUDA-core form, same plan and partials.  kFused: the one-launch step.
+template <int G, bool kFused = false>
 __global__ void __launch_bounds__(kW * 32, 3)
     decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
                       const __grid_constant__ CUtensorMap mv) {
@@ -430,7 +522,12 @@ __global__ void __launch_bounds__(kW * 32, 3)
     u.lo = lo;
     u.slot = part;
     u.np_a = u.np_b = n_parts;
-    unit_body<G, G>(p, &mk, &mv, aligned_smem(smem_raw), &aborted, u);
+    if constexpr (kFused) {
+        __shared__ StepRow step;
+        unit_body<G, G, true>(p, &mk, &mv, aligned_smem(smem_raw), &aborted, u, &step);
+    } else {
+        unit_body<G, G>(p, &mk, &mv, aligned_smem(smem_raw), &aborted, u);
+    }
 }
 
 // ---------------------------------------------------------------- shared prefixes

@@ -140,12 +140,32 @@ def test_reference_arm_prints_contract_line():
 def test_recorded_traffic_is_dropped_when_the_sources_change(monkeypatch):
     import json as _json
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-        rec = _json.load(f)["decode_partition_kernel"]["decode_gqa"]
+        records = _json.load(f)
+    kernel = sorted(records)[0]
+    workload = sorted(records[kernel])[0]
+    rec = records[kernel][workload]
     monkeypatch.setattr(bench, "kernel_source_hash", lambda k: rec["source_hash"])
-    assert bench.recorded_traffic("decode_partition_kernel", "decode_gqa") == \
-        rec["dram_bytes_per_launch"]
+    assert bench.recorded_traffic(kernel, workload) == rec["dram_bytes_per_launch"]
     monkeypatch.setattr(bench, "kernel_source_hash", lambda k: "0" * 16)
-    assert bench.recorded_traffic("decode_partition_kernel", "decode_gqa") is None
-    assert bench.recorded_traffic("decode_partition_kernel", "no_such_workload") is None
-    # a recorded figure is DRAM read + write of one launch
-    assert rec["dram_bytes_per_launch"] == rec["dram_read"] + rec["dram_write"]
+    assert bench.recorded_traffic(kernel, workload) is None
+    assert bench.recorded_traffic(kernel, "no_such_workload") is None
+
+
+def test_recorded_traffic_is_one_launch_of_read_plus_write():
+    import json as _json
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        records = _json.load(f)
+    for kernel, by_workload in records.items():
+        assert kernel in bench.KERNEL_SOURCES, kernel
+        for workload, rec in by_workload.items():
+            captured = rec["dram_read"] + rec["dram_write"]
+            if rec.get("captured_scale", 1.0) == 1.0:
+                assert rec["dram_bytes_per_launch"] == captured, (kernel, workload)
+            else:  # a smaller case scaled to the full workload by its bytes
+                assert rec["dram_bytes_per_launch"] > captured, (kernel, workload)
+
+
+def test_kernel_source_hash_covers_device_code_only():
+    h = bench.kernel_source_hash("decode_mma_kernel")
+    assert len(h) == 16 and h == bench.kernel_source_hash("decode_mma_kernel")
+    assert h != bench.kernel_source_hash("decode_partition_kernel")

@@ -248,10 +248,16 @@ def decode_gqa_fp8(scale: float = 1.0) -> Workload:
     return with_fp8_pages(decode_gqa(scale))
 
 
+def decode_long_shared_fp8(scale: float = 1.0) -> Workload:
+    """The long shared-prefix decode batch with FP8 (E4M3) pages."""
+    return with_fp8_pages(decode_long_shared(scale))
+
+
 WORKLOADS = {
     "decode_tiny": decode_tiny,
     "decode_gqa": decode_gqa,
     "decode_gqa_fp8": decode_gqa_fp8,
+    "decode_long_shared_fp8": decode_long_shared_fp8,
     "decode_mha": decode_mha,
     "decode_long_shared": decode_long_shared,
     "prefill": prefill,
