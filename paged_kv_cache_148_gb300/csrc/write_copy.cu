@@ -14,7 +14,9 @@
 
 namespace pa {
 
-// One thread per 16-byte vector of a (token, kv-head) row, K and V together.
+// A thread moves U consecutive 16-byte vectors of one (token, kv-head) row of
+// K and of V (U divides the row's vectors), all loads issued before the stores.
+template <int U>
 __global__ void __launch_bounds__(256) write_kv_kernel(
     uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, const uint4* __restrict__ k_new,
     const uint4* __restrict__ v_new, const int64_t* __restrict__ slot_mapping, int64_t total_vecs,
@@ -23,11 +25,17 @@ __global__ void __launch_bounds__(256) write_kv_kernel(
     griddep_wait();
     griddep_launch();  // the attention kernel that follows may start launching
     const int64_t per_token = (int64_t)row_vecs * num_kv_heads;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total_vecs;
-         i += (int64_t)gridDim.x * blockDim.x) {
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * U; i < total_vecs;
+         i += (int64_t)gridDim.x * blockDim.x * U) {
         const int64_t t = i / per_token;
         const int64_t r = i - t * per_token;          // h * row_vecs + vec
         const int64_t slot = __ldg(slot_mapping + t);
+        uint4 kx[U], vx[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            kx[u] = __ldg(k_new + i + u);
+            vx[u] = __ldg(v_new + i + u);
+        }
         if (slot < 0 || slot >= num_slots) {
             if (r == 0) set_error(d_err, PA_ERR_OUT_OF_RANGE);
             continue;
@@ -35,10 +43,11 @@ __global__ void __launch_bounds__(256) write_kv_kernel(
         const int64_t blk = slot / block_size, off = slot - blk * block_size;
         const int64_t h = r / row_vecs, vec = r - h * row_vecs;
         const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * row_vecs + vec;
-        const uint4 kx = __ldg(k_new + i);
-        const uint4 vx = __ldg(v_new + i);
-        k_pool[dst] = kx;
-        v_pool[dst] = vx;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            k_pool[dst + u] = kx[u];
+            v_pool[dst + u] = vx[u];
+        }
     }
 }
 
@@ -87,8 +96,11 @@ __global__ void __launch_bounds__(256) write_kv_fp8_kernel(
     }
 }
 
-// grid.x = pair, grid.y = slices of the page; each thread copies vectors of
-// the page with a stride of the slice width.
+// grid.x = pair, grid.y = slices of the page; each thread copies kCopyU
+// vectors of K and kCopyU of V per round (stride: the slice width), all eight
+// loads issued before the stores.
+constexpr int kCopyU = 4;
+
 __global__ void __launch_bounds__(256) copy_blocks_kernel(
     uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, const int32_t* __restrict__ src,
     const int32_t* __restrict__ dst, int64_t page_vecs, int32_t num_blocks, float* k_scale,
@@ -109,18 +121,25 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(
     uint4* kd = k_pool + (int64_t)d * page_vecs;
     uint4* vd = v_pool + (int64_t)d * page_vecs;
     const int64_t step = (int64_t)gridDim.y * blockDim.x;
-    int64_t v = (int64_t)blockIdx.y * blockDim.x + threadIdx.x;
-    // two vectors of K and two of V in flight per iteration
-    for (; v + step < page_vecs; v += 2 * step) {
-        const uint4 a = ks[v], b = ks[v + step], c = vs[v], e = vs[v + step];
-        kd[v] = a;
-        kd[v + step] = b;
-        vd[v] = c;
-        vd[v + step] = e;
-    }
-    if (v < page_vecs) {
-        kd[v] = ks[v];
-        vd[v] = vs[v];
+    for (int64_t v = (int64_t)blockIdx.y * blockDim.x + threadIdx.x; v < page_vecs;
+         v += kCopyU * step) {
+        uint4 a[kCopyU], c[kCopyU];
+#pragma unroll
+        for (int u = 0; u < kCopyU; ++u) {
+            const int64_t w = v + u * step;
+            if (w < page_vecs) {
+                a[u] = ks[w];
+                c[u] = vs[w];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyU; ++u) {
+            const int64_t w = v + u * step;
+            if (w < page_vecs) {
+                kd[w] = a[u];
+                vd[w] = c[u];
+            }
+        }
     }
 }
 
@@ -164,12 +183,14 @@ extern "C" pa_status pa_write_kv(const pa_kv_pool* pool, const void* k_new, cons
     const int32_t row_vecs = (int32_t)(row_bytes / 16);
     const int64_t total = (int64_t)num_tokens * pool->num_kv_heads * row_vecs;
     const int threads = 256;
-    int64_t blocks = (total + threads - 1) / threads;
+    const int U = row_vecs % 4 == 0 ? 4 : 1;  // vectors per thread, within one row
+    int64_t blocks = (total / U + threads - 1) / threads;
     if (blocks > 1048576) blocks = 1048576;
     // dependent launch: the kernel waits (griddep_wait) for the previous kernel
     // in the stream before it writes, but its launch overlaps that kernel's tail
     cudaError_t e = launch_pdl(
-        write_kv_kernel, dim3((unsigned)blocks), dim3(threads), 0, (cudaStream_t)stream,
+        U == 4 ? write_kv_kernel<4> : write_kv_kernel<1>, dim3((unsigned)blocks), dim3(threads), 0,
+        (cudaStream_t)stream,
         (uint4*)pool->k_pool, (uint4*)pool->v_pool, (const uint4*)k_new, (const uint4*)v_new,
         slot_mapping, total, row_vecs, pool->num_kv_heads, pool->block_size,
         (int64_t)pool->num_blocks * pool->block_size, d_err);
@@ -194,7 +215,7 @@ extern "C" pa_status pa_copy_blocks(const pa_kv_pool* pool, const int32_t* src,
     if (!aligned16(pool->k_pool) || !aligned16(pool->v_pool)) return PA_ERR_INVALID_ARG;
     const int64_t page_vecs = page_bytes / 16;
     const int threads = 256;
-    int64_t slices = (page_vecs + threads * 4 - 1) / (threads * 4);
+    int64_t slices = (page_vecs + threads * kCopyU - 1) / (threads * kCopyU);
     if (slices < 1) slices = 1;
     if (slices > 65535) slices = 65535;
     dim3 grid((unsigned)n, (unsigned)slices);
