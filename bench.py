@@ -60,7 +60,7 @@ def flush_l2(buf, i: int):
     back now rather than inside the next timed kernel."""
     import torch
     buf.fill_(i & 255)
-    buf.view(torch.int32).sum()
+    buf.view(torch.int64).sum()  # int64: the sum needs no widened copy of the buffer
 
 
 def parse():
@@ -217,7 +217,7 @@ KERNEL_SOURCES = {
     "decode_step": (_DECODE_DEVICE, "decode_mma.cuh", "tcgen05.cuh", "common.cuh"),
     "decode_mma_kernel": (_DECODE_DEVICE, "decode_mma.cuh", "tcgen05.cuh", "common.cuh"),
     "decode_shared_kernel": (_DECODE_DEVICE, "decode_mma.cuh", "tcgen05.cuh", "common.cuh"),
-    "decode_fp8_mma_kernel": (_DECODE_DEVICE, "decode_mma_fp8.cuh", "common.cuh"),
+    "decode_fp8_mma_kernel": (_DECODE_DEVICE, "decode_mma_fp8.cuh", "tcgen05.cuh", "common.cuh"),
     "prefill_kernel": ("prefill.cu", "tcgen05.cuh", "common.cuh"),
 }
 

@@ -1086,11 +1086,22 @@ static pa_status launch_partial_mma(const pa_kv_pool* pool, const DecodeParams& 
 static bool use_mma_fp8(const pa_kv_pool* pool, int32_t Hq) {
     const int G = pool->num_kv_heads > 0 ? Hq / pool->num_kv_heads : 1;
     return pool->dtype == PA_DTYPE_FP8_E4M3 && pool->head_dim == mma8::kD &&
-           pool->block_size >= 16 && G == 8;
+           pool->block_size >= 16 && G == 8 &&
+           (int64_t)pool->num_blocks * pool->num_kv_heads * pool->block_size <= INT32_MAX;
 }
 
-static pa_status launch_partial_mma_fp8(const DecodeParams& prm, int32_t B, int32_t Hkv,
-                                        int32_t max_parts, cudaStream_t stream) {
+static pa_status launch_partial_mma_fp8(const pa_kv_pool* pool, const DecodeParams& prm,
+                                        int32_t B, int32_t Hkv, int32_t max_parts,
+                                        cudaStream_t stream) {
+    // the pools as [rows][128] codes, boxes of 16 rows in the 128-byte swizzle
+    CUtensorMap mk, mv;
+    const uint64_t rows = (uint64_t)pool->num_blocks * pool->num_kv_heads * pool->block_size;
+    const uint64_t dims[2] = {(uint64_t)mma8::kD, rows};
+    const uint64_t strides[1] = {(uint64_t)mma8::kD};
+    const uint32_t box[2] = {(uint32_t)mma8::kD, (uint32_t)kChunk};
+    if (!encode_u8_map_sw128(&mk, pool->k_pool, 2, dims, strides, box) ||
+        !encode_u8_map_sw128(&mv, pool->v_pool, 2, dims, strides, box))
+        return PA_ERR_CUDA;
     auto kern = mma8::decode_fp8_mma_kernel<8>;
     static bool attr_done[64] = {false};
     int dev = 0;
@@ -1105,7 +1116,7 @@ static pa_status launch_partial_mma_fp8(const DecodeParams& prm, int32_t B, int3
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
     cudaError_t e = launch_pdl(kern, dim3((unsigned)B, (unsigned)Hkv, (unsigned)max_parts),
-                               dim3(mma8::kW * 32), mma8::kSmem, stream, prm);
+                               dim3(mma8::kW * 32), mma8::kSmem, stream, prm, mk, mv);
     if (e != cudaSuccess) {
         record_cuda_error(e);
         return PA_ERR_CUDA;
@@ -1234,7 +1245,7 @@ static pa_status decode_partial_impl(const pa_kv_pool* pool, const void* q, int3
         }
     }
     if (use_mma_fp8(pool, num_q_heads))
-        return launch_partial_mma_fp8(prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
+        return launch_partial_mma_fp8(pool, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
     if (fp8)
         return dispatch_group<uint8_t, false>(G, prm, num_seqs, pool->num_kv_heads, plan.max_parts, cs);
     if (pool->dtype == PA_DTYPE_F32)

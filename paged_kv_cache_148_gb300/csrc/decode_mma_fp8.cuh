@@ -9,10 +9,13 @@
 //
 // Per warp and 16-token chunk, all MMAs are mma.sync m16n8k16 with f16
 // operands and fp32 accumulation (E4M3 -> f16 is exact):
-//   * staging: 16 per-row bulk copies of the K codes into rows padded to
-//     160 bytes (the 8-byte fragment loads are then free of bank conflicts in
-//     natural token order), one 2 KiB bulk copy of the V codes and two
-//     64-byte copies of the chunk's K and V row scales;
+//   * staging: one 2-D TMA box of 16 rows x 128 codes for K and one for V,
+//     from the pools viewed as [rows][128] bytes with the 128-byte swizzle
+//     (row r holds its 16-byte unit u at u ^ (r & 7)), and two 64-byte bulk
+//     copies of the chunk's K and V row scales; tile row r stands for token
+//     ((r & 3) << 1) | (r >> 2) (+8 for the upper half), so the rows one
+//     half-warp reads with the 8-byte K fragment loads have swizzle keys that
+//     differ in bits 1-2 and touch distinct banks;
 //   * S^T = K Q^T: M = 16 tokens, N = 8 heads, K = 16 dims; a lane converts
 //     8 codes of each of its two rows per pair of k-steps
 //     (cvt.rn.f16x2.e4m3x2) straight into its A fragment; Q is converted to
@@ -21,8 +24,9 @@
 //     the exponent: O accumulates p_o = 2^(s + lg2 v_scale - m') with its own
 //     running max m', the sum l uses p = 2^(s - m), so the f16 P operand holds
 //     values near 1 for the terms that matter whatever the scale's magnitude;
-//   * the warp converts the chunk's V codes into a per-warp f16 buffer (rows
-//     of 272 bytes, rows outside the visible range zeroed), and O^T += V^T P^T
+//   * the warp converts the chunk's V codes into a per-warp f16 buffer, each
+//     token into its tile row (rows of 272 bytes, rows outside the visible
+//     range zeroed), and O^T += V^T P^T
 //     runs as in the bf16 kernel (ldmatrix.x4.trans for V^T, movmatrix for
 //     P^T, P split into f16 high + low parts);
 //   * at the end acc = o * 2^(m' - m), so the CTA combine and the merge see
@@ -33,19 +37,24 @@ namespace pa {
 namespace mma8 {
 
 constexpr int kD = 128;
-constexpr int kKPad = 160;                         // K code row stride in shared memory
+constexpr int kBox = kChunk * 128;                 // one TMA box: 16 rows x 128 codes
+constexpr int kScaleOff = 2 * kBox;                // K box | V box | K scales | V scales
+constexpr int kStageBytes = 5 * 1024;              // 4224 used, 1024-aligned boxes
 constexpr int kVPad = 272;                         // f16 V row stride in shared memory
-constexpr int kKBytes = kChunk * kKPad;            // 2560
-constexpr int kVBytes = kChunk * 128;              // 2048 (codes, unpadded)
-constexpr int kStageBytes = kKBytes + kVBytes + 2 * kChunk * 4;  // + K and V scales = 4736
 constexpr int kVBuf = kChunk * kVPad;              // per-warp f16 V buffer, 4352
 constexpr int kW = 4, kS = 2;
 constexpr size_t kRing = (size_t)kW * kS * kStageBytes;
 constexpr size_t kBufs = kRing;                    // kW f16 V buffers
 constexpr size_t kBars = kBufs + (size_t)kW * kVBuf;
 constexpr size_t kMasks = kBars + (size_t)kW * kS * 8;
-constexpr size_t kSmem = kMasks + (size_t)kW * kS * 4;
-static_assert(kStageBytes % 16 == 0 && kVBuf % 16 == 0, "bulk copy and ldmatrix alignment");
+constexpr size_t kSmem = 1024 + kMasks + (size_t)kW * kS * 4;
+static_assert(kVBuf % 16 == 0, "ldmatrix alignment");
+
+// token held by tile row r (r < 8); row r + 8 holds token 8 + tile_tok(r).  The
+// rows an 8-byte K fragment load reads in one half-warp (r = 0-3 or 4-7) then
+// have swizzle keys that differ in bits 1-2, so its 8 units hit distinct banks
+PA_DEVICE int tile_tok(int r) { return ((r & 3) << 1) | (r >> 2); }
+PA_DEVICE int tok_tile(int t) { return (t >> 1) | ((t & 1) << 2); }
 
 PA_DEVICE void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                              uint32_t b0, uint32_t b1) {
@@ -118,7 +127,9 @@ PA_DEVICE float lg2_approx(float x) {
 }
 
 template <int G>
-__global__ void __launch_bounds__(kW * 32) decode_fp8_mma_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kW * 32)
+    decode_fp8_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
+                          const __grid_constant__ CUtensorMap mv) {
     static_assert(G >= 1 && G <= 8, "the heads of a group are the N columns of one tile");
     const int s = blockIdx.x, h = blockIdx.y, part = blockIdx.z;
     griddep_wait();
@@ -146,51 +157,49 @@ __global__ void __launch_bounds__(kW * 32) decode_fp8_mma_kernel(const DecodePar
     int32_t id_reg = table_id(lane);
     int id_base = 0;
 
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* ring = smem + (size_t)warp * kS * kStageBytes;
     unsigned char* vbuf = smem + kBufs + (size_t)warp * kVBuf;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBars) + warp * kS;
     uint32_t* masks = reinterpret_cast<uint32_t*>(smem + kMasks) + warp * kS;
     __shared__ int aborted;
-    if (threadIdx.x == 0) aborted = 0;
+    if (threadIdx.x == 0) {
+        aborted = 0;
+        tc::prefetch_tmap(&mk);
+        tc::prefetch_tmap(&mv);
+    }
     if (lane == 0) {
         for (int i = 0; i < kS; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
     }
     __syncthreads();
 
-    // warp-wide issue of chunk i (a chunk lies in one page): lanes 0-15 copy
-    // the K code rows into padded rows, lane 16 the 16 V code rows, lanes 17
-    // and 18 the K and V row scales
+    // lane 0 issues chunk i (a chunk lies in one page): one box of 16 K code
+    // rows, one of 16 V code rows, and the chunk's K and V row scales
     auto issue = [&](int i, int32_t id) {
         const int stage = i % kS;
         const int t0 = (first + i * kW) * kChunk;
         const int bp = 1 << p.log2_bp;
         const bool page_ok = id >= 0 && id < p.num_blocks;
-        if (!page_ok && lane == 0)
-            set_error(p.d_err, id < 0 ? PA_ERR_NEGATIVE_BLOCK : PA_ERR_OUT_OF_RANGE);
+        if (!page_ok) set_error(p.d_err, id < 0 ? PA_ERR_NEGATIVE_BLOCK : PA_ERR_OUT_OF_RANGE);
         const int valid = min(kChunk, n - t0);
         uint32_t mask = page_ok ? ((1u << valid) - 1u) : 0u;
-        if (lo > t0) mask &= ~((1u << (lo - t0)) - 1u);
+        if (lo > t0) mask &= ~((1u << min(lo - t0, kChunk)) - 1u);
         uint64_t* bar = &bars[stage];
-        if (lane == 0) {
-            masks[stage] = mask;
-            mbar_arrive_expect_tx(bar, page_ok ? (uint32_t)(kChunk * 128 + kVBytes + 2 * kChunk * 4)
-                                               : 0u);
+        masks[stage] = mask;
+        if (!page_ok) {
+            mbar_arrive_expect_tx(bar, 0);
+            return;
         }
-        __syncwarp();
-        if (!page_ok) return;
+        mbar_arrive_expect_tx(bar, (uint32_t)(2 * kBox + 2 * kChunk * 4));
         const int64_t row0 = ((int64_t)id * p.num_kv_heads + h) * bp + (t0 & (bp - 1));
         unsigned char* st = ring + (size_t)stage * kStageBytes;
-        if (lane < 16) {
-            bulk_g2s(st + lane * kKPad, p.k_pool + (row0 + lane) * 128, 128, bar);
-        } else if (lane == 16) {
-            bulk_g2s(st + kKBytes, p.v_pool + row0 * 128, kVBytes, bar);
-        } else if (lane == 17) {
-            bulk_g2s(st + kKBytes + kVBytes, p.k_scale + row0, kChunk * 4, bar);
-        } else if (lane == 18) {
-            bulk_g2s(st + kKBytes + kVBytes + kChunk * 4, p.v_scale + row0, kChunk * 4, bar);
-        }
+        tc::tma_load_2d(st, &mk, 0, (int32_t)row0, bar);
+        tc::tma_load_2d(st + kBox, &mv, 0, (int32_t)row0, bar);
+        bulk_g2s(st + kScaleOff, p.k_scale + row0, kChunk * 4, bar);
+        bulk_g2s(st + kScaleOff + kChunk * 4, p.v_scale + row0, kChunk * 4, bar);
     };
 
     // Q^T columns in f16: lane (gid, tig) holds dims 32 q + 8 tig .. + 7 of head gid
@@ -210,7 +219,7 @@ __global__ void __launch_bounds__(kW * 32) decode_fp8_mma_kernel(const DecodePar
 #pragma unroll
     for (int i = 0; i < kS; ++i) {
         const int32_t id = __shfl_sync(kFull, id_reg, i & 31);
-        if (i < my_n) issue(i, id);
+        if (lane == 0 && i < my_n) issue(i, id);
     }
 
     float o[8][4];
@@ -219,8 +228,13 @@ __global__ void __launch_bounds__(kW * 32) decode_fp8_mma_kernel(const DecodePar
     float m[2] = {-INFINITY, -INFINITY};   // running maxima of s (for l), heads 2 tig, 2 tig + 1
     float mo[2] = {-INFINITY, -INFINITY};  // running maxima of s + lg2 v_scale (for o)
     float l[2] = {0.f, 0.f};
-    const int ta = gid, tb = 8 + gid;      // natural token order
-    const uint32_t k_lane = ta * kKPad + 8 * tig;
+    const int ta = tile_tok(gid), tb = 8 + tile_tok(gid);  // tokens of tile rows gid, gid + 8
+    // K fragment: k-step pair q reads codes 32q + 8tig .. +7 of rows ta and tb:
+    // 16-byte unit 2q + (tig >> 1) at (unit ^ (ta & 7)), byte 8 (tig & 1) in it
+    uint32_t k_off[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        k_off[q] = ta * 128 + ((((2 * q) + (tig >> 1)) ^ (ta & 7)) << 4) + 8 * (tig & 1);
     // ldmatrix: matrices 0 / 1 = tokens r / 8 + r of dims 16 mt .. + 7, 2 / 3 the next 8 dims
     const uint32_t v_lane = (((lane >> 3) & 1) * 8 + (lane & 7)) * kVPad + (lane >> 4) * 16;
 
@@ -236,34 +250,36 @@ __global__ void __launch_bounds__(kW * 32) decode_fp8_mma_kernel(const DecodePar
         }
         const uint32_t vmask = masks[stage];
         unsigned char* kst = ring + (size_t)stage * kStageBytes;
-        const unsigned char* vst = kst + kKBytes;
-        const float* ksc = reinterpret_cast<const float*>(kst + kKBytes + kVBytes);
+        const unsigned char* vst = kst + kBox;
+        const float* ksc = reinterpret_cast<const float*>(kst + kScaleOff);
         const float* vsc = ksc + kChunk;
 
         // ---- V codes -> f16 buffer (rows outside the mask zeroed: unwritten
         //      slots may hold NaN codes); 8 lanes per row, 16 codes each
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
+            // token r's codes c*16 .. +15 (swizzled unit), to its tile row
             const int idx = j * 32 + lane, r = idx >> 3, c = idx & 7;
             uint4 w0 = make_uint4(0, 0, 0, 0), w1 = make_uint4(0, 0, 0, 0);
             if ((vmask >> r) & 1u) {
-                const uint4 u = lds128(smem_u32(vst) + r * 128 + c * 16);
+                const uint4 u = lds128(smem_u32(vst) + r * 128 + ((c ^ (r & 7)) << 4));
                 w0 = make_uint4(e4m3x2_f16x2(u.x & 0xffffu), e4m3x2_f16x2(u.x >> 16),
                                 e4m3x2_f16x2(u.y & 0xffffu), e4m3x2_f16x2(u.y >> 16));
                 w1 = make_uint4(e4m3x2_f16x2(u.z & 0xffffu), e4m3x2_f16x2(u.z >> 16),
                                 e4m3x2_f16x2(u.w & 0xffffu), e4m3x2_f16x2(u.w >> 16));
             }
-            *reinterpret_cast<uint4*>(vbuf + r * kVPad + c * 32) = w0;
-            *reinterpret_cast<uint4*>(vbuf + r * kVPad + c * 32 + 16) = w1;
+            const int tr = (r & 8) | tok_tile(r & 7);
+            *reinterpret_cast<uint4*>(vbuf + tr * kVPad + c * 32) = w0;
+            *reinterpret_cast<uint4*>(vbuf + tr * kVPad + c * 32 + 16) = w1;
         }
 
         // ---- S^T = K Q^T: codes -> f16 A fragments, 8 k-steps in two chains
-        const uint32_t ka = smem_u32(kst) + k_lane;
+        const uint32_t kb = smem_u32(kst);
         float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const uint2 ua = lds64(ka + 32 * q);              // token ta, dims 32 q + 8 tig ..
-            const uint2 ub = lds64(ka + 8 * kKPad + 32 * q);  // token tb
+            const uint2 ua = lds64(kb + k_off[q]);            // token ta, codes 32 q + 8 tig ..
+            const uint2 ub = lds64(kb + k_off[q] + 8 * 128);  // token tb (same swizzle key)
             const uint32_t a0 = e4m3x2_f16x2(ua.x & 0xffffu), a1 = e4m3x2_f16x2(ua.x >> 16);
             const uint32_t a2 = e4m3x2_f16x2(ua.y & 0xffffu), a3 = e4m3x2_f16x2(ua.y >> 16);
             const uint32_t b0 = e4m3x2_f16x2(ub.x & 0xffffu), b1 = e4m3x2_f16x2(ub.x >> 16);
@@ -345,7 +361,7 @@ __global__ void __launch_bounds__(kW * 32) decode_fp8_mma_kernel(const DecodePar
             id_reg = (id_base + lane < my_n) ? table_id(id_base + lane) : -1;
         }
         const int32_t nid = __shfl_sync(kFull, id_reg, (nxt - id_base) & 31);
-        if (nxt < my_n) issue(nxt, nid);
+        if (lane == 0 && nxt < my_n) issue(nxt, nid);
     }
     if (!ok) aborted = 1;
     griddep_launch();

@@ -40,8 +40,9 @@ int device_sm_count() {
     return cached[dev];
 }
 
-bool encode_bf16_map_sw128(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                           const uint64_t* strides, const uint32_t* box) {
+static bool encode_map_sw128(CUtensorMap* map, CUtensorMapDataType type, const void* base,
+                             int rank, const uint64_t* dims, const uint64_t* strides,
+                             const uint32_t* box) {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -62,10 +63,20 @@ bool encode_bf16_map_sw128(CUtensorMap* map, const void* base, int rank, const u
         bx[i] = box[i];
         if (i > 0) st[i - 1] = strides[i - 1];
     }
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
+    CUresult r = fn(map, type, (cuuint32_t)rank, const_cast<void*>(base),
                     d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool encode_bf16_map_sw128(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides, const uint32_t* box) {
+    return encode_map_sw128(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides, box);
+}
+
+bool encode_u8_map_sw128(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                         const uint64_t* strides, const uint32_t* box) {
+    return encode_map_sw128(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rank, dims, strides, box);
 }
 
 // Refcounted pool of block ids with a LIFO free list.

@@ -56,6 +56,9 @@ int device_sm_count();
 // the driver entry point is missing or refuses the description.
 bool encode_bf16_map_sw128(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                            const uint64_t* strides, const uint32_t* box);
+// The same for byte elements (FP8 codes).
+bool encode_u8_map_sw128(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                         const uint64_t* strides, const uint32_t* box);
 
 // Launch with programmatic stream serialization (the kernel must call
 // griddep_wait() before touching memory its predecessor may write).
