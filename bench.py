@@ -429,6 +429,10 @@ def bench_attention(args, wl, dev, world, mode="split", e2e=False, g=None):
         shared = (partner, shared_lens, torch.empty(max(ws_bytes, 16), dtype=torch.uint8,
                                                     device=dev))
     max_parts = g.max_parts()
+    if is_decode and mode == "shared":
+        # the shared-prefix plan sizes its own partitions; its workspace holds
+        # (max, sum, D values) floats per (sequence, q-head, partition slot)
+        max_parts = ws_bytes // (wl.num_seqs * wl.num_q_heads * (wl.head_dim + 2) * 4)
     ab = algorithmic_bytes(wl, window)
     step_bytes = ab["decode_total"] + ab["write"] if is_decode else ab["kv"] + ab["q"] + ab["out"]
     do_flush = _needs_flush(args, step_bytes)

@@ -923,7 +923,14 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
 // ---------------------------------------------------------------- host side
 constexpr int kWarps = 4;
 constexpr int kStages = 2;
-constexpr int kWaves = 9;
+// The automatic plan sizes partitions so that a batch whose every sequence
+// had max_context tokens would fill kWaves rounds of resident CTAs; real
+// batches are shorter on average, so they run about half as many.  Fewer,
+// longer partitions measured faster on long contexts (less partial traffic,
+// fewer CTA start-ups, whole rounds): 3072 tokens gave 224 us against 237 us
+// at 1728 on 8 sequences of 32K-107K tokens at G = 8, while 4- to 16-way
+// splits of U[128, 4096] contexts at G = 4 all lay within 90-94 us.
+constexpr int kWaves = 5;
 
 // The tensor-core partition kernel (decode_mma.cuh) serves bf16 pools with
 // head_dim 128 and pages of >= 16 tokens (a chunk then lies in one page),
@@ -937,14 +944,16 @@ static bool use_mma(const pa_kv_pool* pool, int32_t Hq) {
            (G == 2 || G == 4 || G == 8);
 }
 
+static bool use_mma_fp8(const pa_kv_pool* pool, int32_t Hq);
+
 // Partition CTAs per SM the plan counts on: 3 (the shared-memory limit of
-// the tensor-core kernel and of 16-bit and f32 rows on the CUDA-core one), 2
-// for the CUDA-core kernel at G = 8, where registers allow only two.  (FP8
+// both tensor-core kernels and of 16-bit and f32 rows on the CUDA-core one),
+// 2 for the CUDA-core kernel at G = 8, where registers allow only two.  (FP8
 // rows at G <= 4 run 4 per SM, but measured fastest with the 3-per-SM plan:
 // more partitions cost more in the merge than they gain in balance.)
 static int ctas_per_sm(const pa_kv_pool* pool, int32_t Hq) {
     const int G = pool->num_kv_heads > 0 ? Hq / pool->num_kv_heads : 1;
-    if (use_mma(pool, Hq)) return 3;
+    if (use_mma(pool, Hq) || use_mma_fp8(pool, Hq)) return 3;
     return G >= 8 ? 2 : 3;
 }
 
@@ -958,7 +967,8 @@ struct Plan {
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static pa_status make_plan(const pa_kv_pool* pool, int32_t B, int32_t Hq, int32_t max_ctx,
-                           int32_t partition_tokens, Plan* plan, int32_t window = 0) {
+                           int32_t partition_tokens, Plan* plan, int32_t window = 0,
+                           int waves = kWaves) {
     if (B < 0 || Hq <= 0 || max_ctx < 0 || window < 0) return PA_ERR_INVALID_ARG;
     int64_t chunks_max = ((int64_t)max_ctx + kChunk - 1) / kChunk;
     // a window of w positions starting anywhere touches at most ceil(w/16) + 1 chunks
@@ -969,7 +979,7 @@ static pa_status make_plan(const pa_kv_pool* pool, int32_t B, int32_t Hq, int32_
         pc = partition_tokens / kChunk;
     } else if (partition_tokens == 0) {
         const int64_t units = (int64_t)B * pool->num_kv_heads;
-        const int64_t target = (int64_t)device_sm_count() * ctas_per_sm(pool, Hq) * kWaves;
+        const int64_t target = (int64_t)device_sm_count() * ctas_per_sm(pool, Hq) * waves;
         pc = (units * chunks_max + target - 1) / (target > 0 ? target : 1);
         if (pc < 2 * kWarps) pc = 2 * kWarps;
         pc = (pc + kWarps - 1) / kWarps * kWarps;
@@ -991,11 +1001,15 @@ static pa_status make_plan(const pa_kv_pool* pool, int32_t B, int32_t Hq, int32_
     return PA_OK;
 }
 
-// Plan of the shared-prefix decode: pa_decode's partition size; splitting a
-// context at the shared length adds at most one slot per sequence.
+// Plan of the shared-prefix decode: partitions sized for 9 rounds of resident
+// CTAs (its pair units carry 2G query columns, so their CTAs run longer, and
+// finer partitions balance them better: 231 us at 1728 tokens against 235 us
+// at 3072 on 8 sequences of 32K-107K tokens at G = 8); splitting a context at
+// the shared length adds at most one slot per sequence.
+constexpr int kSharedWaves = 9;
 static pa_status make_shared_plan(const pa_kv_pool* pool, int32_t B, int32_t Hq, int32_t max_ctx,
                                   int32_t partition_tokens, Plan* plan) {
-    pa_status st = make_plan(pool, B, Hq, max_ctx, partition_tokens, plan, 0);
+    pa_status st = make_plan(pool, B, Hq, max_ctx, partition_tokens, plan, 0, kSharedWaves);
     if (st != PA_OK) return st;
     plan->max_parts += 1;
     const size_t rows = (size_t)B * Hq * plan->max_parts;

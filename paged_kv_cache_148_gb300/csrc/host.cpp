@@ -29,12 +29,12 @@ int device_sm_count() {
     static std::mutex mu;
     static int cached[64] = {0};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
     std::lock_guard<std::mutex> lock(mu);
     if (cached[dev] == 0) {
         int n = 0;
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 148;
+            n = 152;
         cached[dev] = n;
     }
     return cached[dev];
