@@ -12,12 +12,15 @@ Sources (page title, section):
   P3 = "PagedAttention 的原理是什么？它如何降低 KV Cache 的内存浪费？" (offer.aigcbaba.com)
   P4 = "vLLM学习笔记-显存管理之PagedAttention" (amentiraz.github.io)
 
-Pins (tests/test_oracle.py): the worked examples of P2 "Page-table 寻址" and
-P2 "引用计数与尾块 COW" (tests/golden/), the out-of-range failure, refcount and
-copy-on-write invariants (P2 "生命周期与所有权"), paged == contiguous bit
-identity (P1 §4, P3 §五), brute force against a library softmax-attention
-routine on tiny inputs, closed forms (one key, identical keys), split/merge
-equivalence, causal-row == truncated-decode identity, and GQA head mapping.
+Pins (tests/test_oracle.py, tests/test_oracle_fp8.py): the worked examples
+of P2 "Page-table 寻址" and P2 "引用计数与尾块 COW" (tests/golden/), the
+out-of-range failure, refcount and copy-on-write invariants (P2 "生命周期与所有权"),
+paged == contiguous bit identity (P1 §4, P3 §五), brute force against a
+library softmax-attention routine on tiny inputs, closed forms (one key,
+identical keys, a dominant key), split/merge equivalence (also with partition
+maxima 1000 apart), causal-row == truncated-decode identity, and GQA head
+mapping.  tests/test_oracle_mutations.py plants mistakes in a copy of this
+package and checks that each one fails a pin.
 """
 from __future__ import annotations
 

@@ -121,6 +121,22 @@ def test_refcount_and_cow_invariants_random_sequences():
             assert len(held) + len(pool.free) == n_blocks
 
 
+def test_new_block_only_at_the_end_of_the_table():
+    # position len(table) * B_p starts the next logical block; a position at a
+    # block boundary inside the table names a block that is already mapped,
+    # so appending there would break "one physical block per logical block"
+    pool = oracle.BlockPool(8)
+    table = []
+    for length in (0, 4):
+        pool.writable_tail(table, length, 4)
+    before = (list(table), list(pool.refcount), list(pool.free))
+    with pytest.raises(ValueError):
+        pool.writable_tail(table, 4, 4)
+    with pytest.raises(ValueError):
+        pool.writable_tail(table, 16, 4)
+    assert (table, pool.refcount, pool.free) == before
+
+
 def test_release_underflow_is_an_error():
     pool = oracle.BlockPool(4)
     t = []
@@ -266,6 +282,26 @@ def test_split_merge_equals_unsplit(part):
     np.testing.assert_allclose(split, full, rtol=1e-13, atol=1e-14)
 
 
+@pytest.mark.parametrize("first", [True, False])
+def test_split_merge_with_far_apart_partition_maxima(first):
+    # one key scores 1000 above the rest: every partition state must be taken
+    # relative to the largest partition max (e^1000 overflows a double), and
+    # the result is that key's value (the dominant-key closed form)
+    n, D, bp = 12, 4, 4
+    k = np.zeros((3, 1, bp, D))
+    v = np.arange(3 * bp * D, dtype=np.float64).reshape(3, 1, bp, D) / 7.0
+    k[:, 0, :, 1] = np.linspace(-1.0, 1.0, n).reshape(3, bp)
+    hot = 0 if first else n - 1
+    k[hot // bp, 0, hot % bp, 0] = 1000.0
+    q = np.array([[[1.0, 1.0, 0.0, 0.0]]])
+    tables, lens = [[0, 1, 2]], [n]
+    full = oracle.decode(k, v, q, tables, lens, 1.0)
+    split = oracle.decode_split(k, v, q, tables, lens, 1.0, bp)
+    assert np.isfinite(split).all()
+    assert np.array_equal(full[0, 0], v[hot // bp, 0, hot % bp])
+    assert np.array_equal(split[0, 0], v[hot // bp, 0, hot % bp])
+
+
 def test_gqa_head_mapping():
     # q-head g reads kv-head g // G: changing kv-head 1 changes only heads 4..7
     wl, oc, q = _small_case("bf16", 4, 2, 128, 16, [30, 50], seed=51)
@@ -370,14 +406,20 @@ def test_write_rejects_out_of_pool_slot():
     row = np.zeros((1, 1, 8), np.float32)
     with pytest.raises(IndexError):
         oracle.write_kv(k, v, row, row, [8])
+    with pytest.raises(IndexError):
+        oracle.write_kv(k, v, row, row, [-1])
+    assert (k.view(np.uint32) == 0xFFFFFFFF).all()
 
 
 def test_copy_blocks_copies_whole_block():
     k, v = oracle.poisoned_pool(6, 2, 4, 8, "bf16")
-    k[2] = np.arange(64, dtype=np.uint16).reshape(2, 4, 8)
+    src_k = np.arange(64, dtype=np.uint16).reshape(2, 4, 8)
+    k[2] = src_k
     v[2] = 7
     oracle.copy_blocks(k, v, [2], [5])
-    assert np.array_equal(k[5], k[2]) and np.array_equal(v[5], v[2])
+    # dst holds the source's rows and the source is unchanged
+    assert np.array_equal(k[5], src_k) and np.array_equal(k[2], src_k)
+    assert (v[5] == 7).all() and (v[2] == 7).all()
     with pytest.raises(IndexError):
         oracle.copy_blocks(k, v, [0], [6])
 
