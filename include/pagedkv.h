@@ -212,8 +212,15 @@ pa_status pa_decode_workspace_bytes(const pa_kv_pool* pool, int32_t num_seqs,
  * Arithmetic: bf16 pools with D = 128, pages of >= 16 tokens and 2, 4 or 8
  * q-heads per kv-head run the score and P V products on tensor cores
  * (bf16 operands, float32 accumulation; the probabilities enter P V as a
- * bf16 high part plus a bf16 low part, about 16 significant bits); all other
- * shapes run them in float32 on CUDA cores.
+ * bf16 high part plus a bf16 low part, about 16 significant bits).  FP8
+ * pools with pages of >= 16 tokens and 8 q-heads per kv-head run them on
+ * tensor cores with f16 operands: the E4M3 codes convert exactly, the query
+ * is rounded to f16 once (exact for bf16 components of magnitude 2^-14 to
+ * 65280; smaller ones keep an absolute precision of 2^-24; a component of
+ * magnitude 65536 or more overflows and makes that row's output non-finite,
+ * unflagged), the probabilities enter P V as an f16 high + low pair, and
+ * accumulation is float32.  All other shapes run them in float32 on CUDA
+ * cores.
  */
 pa_status pa_decode(const pa_kv_pool* pool, const void* q, int32_t num_q_heads,
                     const int32_t* block_tables, int32_t max_blocks_per_seq,
