@@ -185,6 +185,22 @@ def test_allocator_errors(L):
         pkv.Allocator(3, [0, 0, 1])               # not a permutation
 
 
+def test_new_block_only_at_the_end_of_the_table(L):
+    # a block boundary inside the table or past its end is not the next
+    # block: INVALID_ARG, with the table and the refcounts unchanged (the
+    # oracle's BlockPool rejects the same calls)
+    a = pkv.Allocator(8)
+    t = pkv.BlockTable()
+    for length in (0, 4):
+        a.writable_tail(t, length, 4)
+    before = (t.tolist(), [a.refcount(b) for b in range(8)])
+    for length in (4, 16):
+        with pytest.raises(pkv.PagedKVError) as ei:
+            a.writable_tail(t, length, 4)
+        assert ei.value.status == pkv.PA_ERR_INVALID_ARG
+    assert (t.tolist(), [a.refcount(b) for b in range(8)]) == before
+
+
 def test_device_entry_points_reject_bad_arguments_on_host(L):
     # these return before any CUDA call, so they run without a GPU
     P = ctypes.c_void_p
