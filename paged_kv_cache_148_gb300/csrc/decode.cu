@@ -1002,10 +1002,10 @@ static pa_status make_plan(const pa_kv_pool* pool, int32_t B, int32_t Hq, int32_
 }
 
 // Plan of the shared-prefix decode: partitions sized for 9 rounds of resident
-// CTAs (its pair units carry 2G query columns, so their CTAs run longer, and
-// finer partitions balance them better: 231 us at 1728 tokens against 235 us
-// at 3072 on 8 sequences of 32K-107K tokens at G = 8); splitting a context at
-// the shared length adds at most one slot per sequence.
+// CTAs (its pair units carry 2G query columns, so their CTAs run longer; on 8
+// sequences of 32K-107K tokens at G = 8 the coarser plan gained nothing:
+// 231-236 us per step at 1728 tokens, 235 us at 3072); splitting a context
+// at the shared length adds at most one slot per sequence.
 constexpr int kSharedWaves = 9;
 static pa_status make_shared_plan(const pa_kv_pool* pool, int32_t B, int32_t Hq, int32_t max_ctx,
                                   int32_t partition_tokens, Plan* plan) {
