@@ -1,7 +1,8 @@
 """The oracle's pins catch plausible mistakes in the oracle.
 
 Each case plants one mistake (a dropped term, a wrong sign, index or bound,
-a swapped operand) in a copy of ``oracle/`` made in a temporary directory,
+a swapped operand) in a copy of ``oracle/`` made in a scratch directory of
+the repository (``.oracle_mutants/``, ignored by git, removed afterwards),
 then runs the pin suites (tests/test_oracle.py, tests/test_oracle_fp8.py)
 against that copy in a child process: at least one pin must fail.  A control
 run of the unchanged copy must pass, so a surviving mistake cannot hide
@@ -138,21 +139,34 @@ def _copy_oracle(dst_root, mutant=None):
     return dst_root
 
 
+SCRATCH = os.path.join(ROOT, ".oracle_mutants")
+
+
 def _run_pins(work):
+    tmp = os.path.join(work, "tmp")
+    os.makedirs(tmp, exist_ok=True)
     env = dict(os.environ, PYTHONPATH=os.pathsep.join([work, ROOT]), OMP_NUM_THREADS="2",
-               PYTHONDONTWRITEBYTECODE="1")
+               PYTHONDONTWRITEBYTECODE="1", TMPDIR=tmp)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         *PINS], cwd=work, env=env, capture_output=True, text=True, timeout=600)
     return r.returncode, r.stdout[-1500:] + r.stderr[-1500:]
 
 
-def test_every_planted_mistake_fails_a_pin(tmp_path):
-    control = _copy_oracle(str(tmp_path / "control"))
+@pytest.fixture
+def scratch():
+    shutil.rmtree(SCRATCH, ignore_errors=True)
+    os.makedirs(SCRATCH)
+    yield SCRATCH
+    shutil.rmtree(SCRATCH, ignore_errors=True)
+
+
+def test_every_planted_mistake_fails_a_pin(scratch):
+    control = _copy_oracle(os.path.join(scratch, "control"))
     rc, log = _run_pins(control)
     assert rc == 0, "the unchanged copy of the oracle must pass its pins:\n" + log
 
     def one(i):
-        work = _copy_oracle(str(tmp_path / ("m%02d" % i)), MUTANTS[i])
+        work = _copy_oracle(os.path.join(scratch, "m%02d" % i), MUTANTS[i])
         return i, _run_pins(work)
 
     survivors, crashed = [], []
