@@ -61,7 +61,8 @@ typedef enum {
     PA_DTYPE_F32 = 0,          /* IEEE float32 storage and operands */
     PA_DTYPE_BF16 = 1,         /* bfloat16 storage and operands, float32 accumulation */
     PA_DTYPE_FP8_E4M3 = 2      /* FP8 E4M3 pages with one float32 scale per (token, kv-head)
-                                  row; new rows arrive as bf16, attention runs in float32 */
+                                  row; new rows arrive as bf16, attention accumulates in
+                                  float32 (operand precision: see pa_decode) */
 } pa_dtype;
 
 /*
