@@ -137,6 +137,16 @@ def test_reference_arm_prints_contract_line():
     assert line["cpu_baseline"]["kind"] == "oracle"
 
 
+def test_reference_arm_runs_on_rank_0_only():
+    # under torchrun every rank but 0 exits at once, printing nothing
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--workload", "decode_tiny", "--steps", "3", "--warmup",
+                        "1"], capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
+
+
 def test_recorded_traffic_is_dropped_when_the_sources_change(monkeypatch):
     import json as _json
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
