@@ -127,7 +127,7 @@ def test_prefill_flags_table_entry_outside_pool():
 # --------------------------------------------------------------------------- V range
 def _rescale_v(g, oc, picks, factor):
     """Replace the V rows of the (sequence, position) picks by factor x their
-    value, rounded to bf16, in the GPU pool (through pa_write_kv) and in the
+    value, rounded to bf16, in the device-resident KV pool (through pa_write_kv) and in the
     oracle's pool; K rows are rewritten unchanged."""
     Bp = g.wl.block_size
     gt = g.tables_list()
